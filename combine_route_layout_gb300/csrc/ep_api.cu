@@ -1,0 +1,673 @@
+// libep host library: the C ABI declared in include/ep.h.
+//
+// Validates the EpDispatchCombineConfig-style config (MORI-EP User Guide,
+// section 2), carves the caller's workspace, keeps the dispatch/combine/reset
+// state machine of section 3 (reset() must separate iterations unless
+// combine is called with call_reset), and enqueues the kernels. No function
+// here allocates device memory or blocks the host, except ep_sync.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "ep_kernels.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ep_status fail(ep_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+ep_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(EP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+enum State { kReady = 0, kDispatched = 1, kCombined = 2 };
+
+int dtype_size(int dt) {
+  switch (dt) {
+    case EP_DTYPE_BF16: return 2;
+    case EP_DTYPE_FP32: return 4;
+    case EP_DTYPE_FP8_E4M3: return 1;
+    default: return 0;
+  }
+}
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Sizes derived from a config.
+struct Geometry {
+  int R, H, k, E_r, E, Tmax;
+  int64_t cap, pcap;
+  int cpr, nchunks, cpr_recv, nchunks_recv;
+  bool quant, std_moe;
+  int64_t in_row_bytes, out_row_bytes;
+  int scale_row_bytes;       // received scale row bytes (0 = none)
+  int in_scale_row_bytes;    // pass-through input scale row bytes
+};
+
+// Workspace pointers (or offsets when base == nullptr).
+struct Carve {
+  int32_t* err;
+  unsigned int* tickets;     // [4]
+  uint32_t* mask;
+  uint8_t* local8;
+  int32_t* chunk_cnt2d;
+  int32_t* chunk_off2d;
+  int32_t* recv_num_token;
+  int32_t* slot_map;
+  int32_t* src_pos;
+  uint8_t* recv_x;
+  uint8_t* recv_scales;
+  float* recv_w;
+  int32_t* recv_idx;
+  uint16_t* local16;
+  int32_t* chunk_cnt_std;
+  int32_t* chunk_off_std;
+  int32_t* expert_count;
+  int32_t* expert_offset;
+  int32_t* rank_rows;
+  int64_t* layout_range;
+  int32_t* row_map;
+  int32_t* packed_src_info;
+  uint8_t* packed_x;
+  uint8_t* packed_scales;
+  uint16_t* conv_local16;
+  int32_t* conv_chunk_cnt;
+  int32_t* conv_chunk_off;
+  size_t total;
+};
+
+template <typename T>
+void take(uint8_t* base, size_t& off, T*& ptr, size_t bytes) {
+  ptr = reinterpret_cast<T*>(base ? base + off : nullptr);
+  off = align_up(off + bytes);
+}
+
+Carve carve(const Geometry& g, uint8_t* base) {
+  Carve c{};
+  size_t off = 0;
+  const int64_t R = g.R, T = g.Tmax, k = g.k;
+  take(base, off, c.err, 4 * sizeof(int32_t));
+  take(base, off, c.tickets, 4 * sizeof(unsigned int));
+  take(base, off, c.mask, R * T * 4);
+  take(base, off, c.local8, R * T * R);
+  take(base, off, c.chunk_cnt2d, (size_t)g.nchunks * R * 4);
+  take(base, off, c.chunk_off2d, (size_t)g.nchunks * R * 4);
+  take(base, off, c.recv_num_token, R * 4);
+  take(base, off, c.slot_map, R * T * R * 4);
+  take(base, off, c.src_pos, R * g.cap * 4);
+  take(base, off, c.recv_x, R * g.cap * g.out_row_bytes);
+  take(base, off, c.recv_scales, R * g.cap * g.scale_row_bytes);
+  take(base, off, c.recv_w, R * g.cap * k * 4);
+  take(base, off, c.recv_idx, R * g.cap * k * 4);
+  if (g.std_moe) {
+    take(base, off, c.local16, R * T * k * 2);
+    take(base, off, c.chunk_cnt_std, (size_t)g.nchunks * g.E * 4);
+    take(base, off, c.chunk_off_std, (size_t)g.nchunks * g.E * 4);
+    take(base, off, c.expert_count, (size_t)g.E * 4);
+    take(base, off, c.expert_offset, (size_t)g.E * 4);
+    take(base, off, c.rank_rows, R * 4);
+    take(base, off, c.layout_range, (size_t)g.E * R * 8);
+    take(base, off, c.row_map, R * T * k * 4);
+    take(base, off, c.packed_src_info, R * g.pcap * 4);
+    take(base, off, c.packed_x, R * g.pcap * g.out_row_bytes);
+    take(base, off, c.packed_scales, R * g.pcap * g.scale_row_bytes);
+    take(base, off, c.conv_local16, R * g.cap * k * 2);
+    take(base, off, c.conv_chunk_cnt, (size_t)g.nchunks_recv * g.E_r * 4);
+    take(base, off, c.conv_chunk_off, (size_t)g.nchunks_recv * g.E_r * 4);
+  }
+  c.total = off;
+  return c;
+}
+
+ep_status make_geometry(const ep_config* cfg, Geometry* g) {
+  if (!cfg) return fail(EP_ERR_INVALID_ARG, "config is NULL");
+  const int R = cfg->world_size, H = cfg->hidden_dim, k = cfg->num_experts_per_token;
+  const int E_r = cfg->num_experts_per_rank, T = cfg->max_num_inp_token_per_rank;
+  if (R < 1 || R > EP_MAX_WORLD_SIZE)
+    return fail(EP_ERR_INVALID_ARG, "world_size %d outside [1, %d]", R, EP_MAX_WORLD_SIZE);
+  if (H < 8 || H % 8 != 0) return fail(EP_ERR_INVALID_ARG, "hidden_dim %d must be a positive multiple of 8", H);
+  if (k < 1 || k > EP_MAX_TOPK)
+    return fail(EP_ERR_INVALID_ARG, "num_experts_per_token %d outside [1, %d]", k, EP_MAX_TOPK);
+  if (E_r < 1 || (int64_t)R * E_r > EP_MAX_EXPERTS)
+    return fail(EP_ERR_INVALID_ARG, "world_size * num_experts_per_rank must be in [1, %d]",
+                EP_MAX_EXPERTS);
+  if (T < 1) return fail(EP_ERR_INVALID_ARG, "max_num_inp_token_per_rank must be >= 1");
+  if ((int64_t)R * R * T > INT32_MAX)
+    return fail(EP_ERR_INVALID_ARG, "world_size^2 * max tokens exceeds the int32 src_token_pos range");
+  const int in_sz = dtype_size(cfg->data_type);
+  if (in_sz == 0) return fail(EP_ERR_INVALID_ARG, "unknown data_type %d", cfg->data_type);
+  if (cfg->quant_type != EP_QUANT_NONE && cfg->quant_type != EP_QUANT_FP8_E4M3_BLOCK128)
+    return fail(EP_ERR_INVALID_ARG, "unknown quant_type %d", cfg->quant_type);
+  const bool quant = cfg->quant_type == EP_QUANT_FP8_E4M3_BLOCK128;
+  if (cfg->combine_dtype != EP_DTYPE_BF16 && cfg->combine_dtype != EP_DTYPE_FP32)
+    return fail(EP_ERR_INVALID_ARG, "combine_dtype must be BF16 or FP32");
+  if (cfg->combine_out_dtype != EP_DTYPE_BF16 && cfg->combine_out_dtype != EP_DTYPE_FP32)
+    return fail(EP_ERR_INVALID_ARG, "combine_out_dtype must be BF16 or FP32");
+  if (cfg->scale_dim < 0) return fail(EP_ERR_INVALID_ARG, "scale_dim must be >= 0");
+  if (cfg->scale_dim > 0 && cfg->scale_type_size != 1 && cfg->scale_type_size != 2 &&
+      cfg->scale_type_size != 4 && cfg->scale_type_size != 8)
+    return fail(EP_ERR_INVALID_ARG, "scale_type_size must be 1, 2, 4 or 8");
+  if (cfg->warp_num_per_block > 8)
+    return fail(EP_ERR_INVALID_ARG, "warp_num_per_block must be <= 8");
+  Geometry x{};
+  x.R = R; x.H = H; x.k = k; x.E_r = E_r; x.E = R * E_r; x.Tmax = T;
+  x.cap = (int64_t)R * T;
+  x.cpr = (T + ep::kChunk - 1) / ep::kChunk;
+  x.nchunks = R * x.cpr;
+  x.cpr_recv = (int)((x.cap + ep::kChunk - 1) / ep::kChunk);
+  x.nchunks_recv = R * x.cpr_recv;
+  x.quant = quant;
+  x.std_moe = cfg->standard_moe != 0;
+  x.in_row_bytes = (int64_t)H * in_sz;
+  if (x.in_row_bytes % 16 != 0)
+    return fail(EP_ERR_INVALID_ARG, "hidden_dim * element size must be a multiple of 16 bytes");
+  if (quant) {
+    if (cfg->data_type != EP_DTYPE_BF16)
+      return fail(EP_ERR_INVALID_ARG, "FP8 block quantisation needs BF16 input");
+    if (H % EP_QUANT_BLOCK != 0)
+      return fail(EP_ERR_INVALID_ARG, "FP8 block quantisation needs hidden_dim %% 128 == 0");
+    if (cfg->scale_dim != 0 && !(cfg->scale_dim == H / EP_QUANT_BLOCK && cfg->scale_type_size == 4))
+      return fail(EP_ERR_INVALID_ARG, "with FP8 block quantisation scale_dim must be 0 or hidden_dim/128 (4-byte)");
+    x.out_row_bytes = H;
+    x.scale_row_bytes = H / EP_QUANT_BLOCK * 4;
+    x.in_scale_row_bytes = 0;
+  } else {
+    x.out_row_bytes = x.in_row_bytes;
+    x.scale_row_bytes = cfg->scale_dim * (cfg->scale_dim > 0 ? cfg->scale_type_size : 0);
+    x.in_scale_row_bytes = x.scale_row_bytes;
+  }
+  if (x.std_moe) {
+    const int64_t worst = (int64_t)R * T * std::min(k, E_r) + (int64_t)(ep::kPadRows - 1) * E_r;
+    x.pcap = cfg->max_packed_rows_per_rank > 0 ? cfg->max_packed_rows_per_rank : worst;
+    if ((int64_t)R * x.pcap > INT32_MAX)
+      return fail(EP_ERR_INVALID_ARG, "world_size * packed rows per rank exceeds int32");
+  } else {
+    x.pcap = 0;
+  }
+  *g = x;
+  return EP_OK;
+}
+
+ep_status device_sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  *out = n;
+  return EP_OK;
+}
+
+}  // namespace
+
+struct ep_handle {
+  ep_config cfg;
+  Geometry g;
+  Carve w;
+  uint8_t* ws;
+  size_t ws_bytes;
+  int state;
+  bool has2d, hasstd, needs_init;
+  int ntok[EP_MAX_WORLD_SIZE];
+  int sm_count;
+};
+
+namespace {
+
+ep_status ensure_ready_device(ep_handle* h, cudaStream_t st) {
+  if (h->sm_count == 0) {
+    ep_status s = device_sm_count(&h->sm_count);
+    if (s != EP_OK) return s;
+  }
+  if (h->needs_init) {
+    cudaError_t e = cudaMemsetAsync(h->w.err, 0, 4 * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->w.tickets, 0, 4 * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    h->needs_init = false;
+  }
+  return EP_OK;
+}
+
+int block_threads(const ep_handle* h) {
+  const int w = h->cfg.warp_num_per_block > 0 ? h->cfg.warp_num_per_block : 8;
+  return w * 32;
+}
+
+ep::LaunchCfg launch_cfg(const ep_handle* h) {
+  ep::LaunchCfg lc;
+  lc.grid_hint = h->cfg.block_num;
+  lc.block = block_threads(h);
+  lc.sm_count = h->sm_count;
+  return lc;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ep_status check_tokens(ep_handle* h, const int32_t* num_tokens) {
+  if (!num_tokens) return fail(EP_ERR_INVALID_ARG, "num_tokens is NULL");
+  for (int s = 0; s < h->g.R; ++s)
+    if (num_tokens[s] < 0 || num_tokens[s] > h->g.Tmax)
+      return fail(EP_ERR_INVALID_ARG, "num_tokens[%d] = %d outside [0, %d]", s, num_tokens[s],
+                  h->g.Tmax);
+  return EP_OK;
+}
+
+ep_status check_dispatch_inputs(ep_handle* h, const void* x, const float* w, const void* scales,
+                                const int32_t* idx) {
+  if (!x || !w || !idx) return fail(EP_ERR_INVALID_ARG, "x, weights and indices must be non-NULL");
+  if (!aligned(x, 16)) return fail(EP_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  if (!aligned(w, 4) || !aligned(idx, 4))
+    return fail(EP_ERR_INVALID_ARG, "weights and indices must be 4-byte aligned");
+  if (h->g.quant && scales)
+    return fail(EP_ERR_INVALID_ARG, "scales must be NULL with FP8 block quantisation");
+  if (!h->g.quant && h->g.in_scale_row_bytes > 0 && !scales)
+    return fail(EP_ERR_INVALID_ARG, "scale_dim > 0 needs a scales array");
+  if (scales && (h->g.in_scale_row_bytes % 4 == 0) && !aligned(scales, 4))
+    return fail(EP_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  return EP_OK;
+}
+
+void fill_layout_common(ep_handle* h, const int32_t* idx, ep::LayoutParams* p) {
+  const Geometry& g = h->g;
+  memset(p, 0, sizeof(*p));
+  p->R = g.R; p->Tmax = g.Tmax; p->k = g.k; p->E_r = g.E_r; p->E = g.E;
+  p->cpr = g.cpr; p->nchunks = g.nchunks;
+  for (int s = 0; s < g.R; ++s) p->ntok[s] = h->ntok[s];
+  p->idx = idx;
+  p->err = h->w.err;
+}
+
+void fill_dispatch_common(ep_handle* h, const void* x, const float* w, const void* scales,
+                          const int32_t* idx, ep::DispatchParams* p) {
+  const Geometry& g = h->g;
+  memset(p, 0, sizeof(*p));
+  p->R = g.R; p->Tmax = g.Tmax; p->k = g.k; p->E_r = g.E_r; p->E = g.E; p->cpr = g.cpr;
+  for (int s = 0; s < g.R; ++s) p->ntok[s] = h->ntok[s];
+  p->H = g.H;
+  p->in_row_bytes = g.in_row_bytes;
+  p->out_row_bytes = g.out_row_bytes;
+  p->scale_row_bytes = g.quant ? 0 : g.in_scale_row_bytes;
+  const int64_t step = g.quant ? (int64_t)ep::kQuantUnroll * 512 * 2
+                               : (int64_t)ep::kCopyUnroll * 512;  // source bytes per unit
+  p->segs_per_token = (int)((g.in_row_bytes + step - 1) / step);
+  p->total_units = (int64_t)g.R * g.Tmax * p->segs_per_token;
+  p->x = static_cast<const uint8_t*>(x);
+  p->w = w;
+  p->idx = idx;
+  p->scales_in = static_cast<const uint8_t*>(scales);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ep_last_error(void) { return g_last_error.c_str(); }
+
+size_t ep_workspace_size(const ep_config* cfg) {
+  Geometry g;
+  if (make_geometry(cfg, &g) != EP_OK) return 0;
+  return carve(g, nullptr).total;
+}
+
+ep_status ep_config_create(const ep_config* cfg, void* d_workspace, size_t workspace_bytes,
+                           ep_handle** out_handle) {
+  if (!out_handle) return fail(EP_ERR_INVALID_ARG, "out_handle is NULL");
+  *out_handle = nullptr;
+  Geometry g;
+  ep_status s = make_geometry(cfg, &g);
+  if (s != EP_OK) return s;
+  const size_t need = carve(g, nullptr).total;
+  if (!d_workspace) return fail(EP_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(d_workspace, kAlign)) return fail(EP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (workspace_bytes < need)
+    return fail(EP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  ep_handle* h = new ep_handle();
+  h->cfg = *cfg;
+  h->g = g;
+  h->ws = static_cast<uint8_t*>(d_workspace);
+  h->ws_bytes = workspace_bytes;
+  h->w = carve(g, h->ws);
+  h->state = kReady;
+  h->has2d = h->hasstd = false;
+  h->needs_init = true;
+  h->sm_count = 0;
+  *out_handle = h;
+  return EP_OK;
+}
+
+void ep_destroy(ep_handle* h) { delete h; }
+
+ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const void* scales,
+                      const int32_t* indices, const int32_t* num_tokens, void* stream,
+                      ep_dispatch_out* out) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (h->state != kReady) return fail(EP_ERR_STATE, "dispatch needs reset() after the previous iteration");
+  ep_status s = check_dispatch_inputs(h, x, weights, scales, indices);
+  if (s == EP_OK) s = check_tokens(h, num_tokens);
+  if (s != EP_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  for (int r = 0; r < h->g.R; ++r) h->ntok[r] = num_tokens[r];
+
+  ep::LayoutParams lp;
+  fill_layout_common(h, indices, &lp);
+  lp.mask = h->w.mask;
+  lp.local8 = h->w.local8;
+  lp.recv_num_token = h->w.recv_num_token;
+  lp.chunk_cnt = h->w.chunk_cnt2d;
+  lp.chunk_off = h->w.chunk_off2d;
+  lp.ticket = h->w.tickets + 0;
+  cudaError_t e = ep::launch_layout_2d(lp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "routing-layout launch");
+
+  ep::DispatchParams dp;
+  fill_dispatch_common(h, x, weights, scales, indices, &dp);
+  dp.cap = h->g.cap;
+  dp.mask = h->w.mask;
+  dp.local8 = h->w.local8;
+  dp.chunk_off = h->w.chunk_off2d;
+  dp.slot_map = h->w.slot_map;
+  dp.src_pos = h->w.src_pos;
+  dp.out_x = h->w.recv_x;
+  dp.out_scales = h->w.recv_scales;
+  dp.out_w = h->w.recv_w;
+  dp.out_idx = h->w.recv_idx;
+  e = ep::launch_dispatch_2d(dp, h->g.quant, launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+
+  h->state = kDispatched;
+  h->has2d = true;
+  h->hasstd = false;
+  if (out) {
+    out->x = h->w.recv_x;
+    out->scales = h->g.scale_row_bytes > 0 ? h->w.recv_scales : nullptr;
+    out->weights = h->w.recv_w;
+    out->indices = h->w.recv_idx;
+    out->recv_num_token = h->w.recv_num_token;
+    out->src_token_pos = h->w.src_pos;
+    out->cap = h->g.cap;
+    out->x_row_bytes = h->g.out_row_bytes;
+    out->scale_row_bytes = h->g.scale_row_bytes;
+  }
+  return EP_OK;
+}
+
+ep_status ep_combine(ep_handle* h, const void* expert_out, const float* weights,
+                     const int32_t* indices, void* out, float* out_weights, int32_t call_reset,
+                     void* stream) {
+  (void)indices;
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->has2d || h->state == kReady) return fail(EP_ERR_STATE, "combine needs a preceding dispatch");
+  if (!expert_out || !out) return fail(EP_ERR_INVALID_ARG, "expert_out and out must be non-NULL");
+  if (!aligned(expert_out, 16) || !aligned(out, 16))
+    return fail(EP_ERR_INVALID_ARG, "expert_out and out must be 16-byte aligned");
+  if ((h->cfg.weighted_combine || out_weights) && !weights)
+    return fail(EP_ERR_INVALID_ARG, "weighted combine and out_weights need weights");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  const Geometry& g = h->g;
+  ep::CombineParams p;
+  memset(&p, 0, sizeof(p));
+  p.R = g.R; p.Tmax = g.Tmax; p.k = g.k; p.E_r = g.E_r; p.H = g.H;
+  for (int r = 0; r < g.R; ++r) p.ntok[r] = h->ntok[r];
+  p.cap = g.cap;
+  p.segs_per_token = (g.H + ep::kCombineUnroll * 256 - 1) / (ep::kCombineUnroll * 256);
+  p.total_units = (int64_t)g.R * g.Tmax * p.segs_per_token;
+  p.weighted = h->cfg.weighted_combine != 0;
+  p.y = static_cast<const uint8_t*>(expert_out);
+  p.w = weights;
+  p.recv_idx = h->w.recv_idx;
+  p.slot_map = h->w.slot_map;
+  p.out = static_cast<uint8_t*>(out);
+  p.out_w = out_weights;
+  cudaError_t e = ep::launch_combine_2d(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
+                                        launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  h->state = kCombined;
+  if (call_reset) return ep_reset(h, stream);
+  return EP_OK;
+}
+
+ep_status ep_get_dispatch_src_token_pos(ep_handle* h, const int32_t** d_src_token_pos) {
+  if (!h || !d_src_token_pos) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+  if (!h->has2d) return fail(EP_ERR_STATE, "no dispatch layout (call ep_dispatch first)");
+  *d_src_token_pos = h->w.src_pos;
+  return EP_OK;
+}
+
+ep_status ep_reset(ep_handle* h, void* stream) {
+  (void)stream;
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  h->state = kReady;
+  h->has2d = h->hasstd = false;
+  return EP_OK;
+}
+
+ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* weights,
+                                   const void* scales, const int32_t* indices,
+                                   const int32_t* num_tokens, void* stream, ep_std_moe_out* out) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->g.std_moe) return fail(EP_ERR_INVALID_ARG, "config has standard_moe = 0");
+  if (h->state != kReady) return fail(EP_ERR_STATE, "dispatch needs reset() after the previous iteration");
+  ep_status s = check_dispatch_inputs(h, x, weights, scales, indices);
+  if (s == EP_OK) s = check_tokens(h, num_tokens);
+  if (s != EP_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  for (int r = 0; r < h->g.R; ++r) h->ntok[r] = num_tokens[r];
+
+  ep::LayoutParams lp;
+  fill_layout_common(h, indices, &lp);
+  lp.local16 = h->w.local16;
+  lp.expert_count = h->w.expert_count;
+  lp.expert_offset = h->w.expert_offset;
+  lp.rank_rows = h->w.rank_rows;
+  lp.layout_range = h->w.layout_range;
+  lp.packed_src_info = h->w.packed_src_info;
+  lp.pcap = h->g.pcap;
+  lp.chunk_cnt = h->w.chunk_cnt_std;
+  lp.chunk_off = h->w.chunk_off_std;
+  lp.ticket = h->w.tickets + 1;
+  cudaError_t e = ep::launch_layout_std(lp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "standard-MoE layout launch");
+
+  ep::DispatchParams dp;
+  fill_dispatch_common(h, x, weights, scales, indices, &dp);
+  dp.cap = h->g.pcap;
+  dp.local16 = h->w.local16;
+  dp.chunk_off = h->w.chunk_off_std;
+  dp.expert_offset = h->w.expert_offset;
+  dp.src_pos = h->w.packed_src_info;
+  dp.row_map = h->w.row_map;
+  dp.out_x = h->w.packed_x;
+  dp.out_scales = h->w.packed_scales;
+  e = ep::launch_dispatch_std(dp, h->g.quant, launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "standard-MoE dispatch launch");
+
+  h->state = kDispatched;
+  h->has2d = false;
+  h->hasstd = true;
+  if (out) {
+    out->packed_x = h->w.packed_x;
+    out->packed_scales = h->g.scale_row_bytes > 0 ? h->w.packed_scales : nullptr;
+    out->packed_count = h->w.expert_count;
+    out->packed_src_info = h->w.packed_src_info;
+    out->packed_layout_range = h->w.layout_range;
+    out->expert_offset = h->w.expert_offset;
+    out->rank_rows = h->w.rank_rows;
+    out->pcap = h->g.pcap;
+    out->x_row_bytes = h->g.out_row_bytes;
+  }
+  return EP_OK;
+}
+
+ep_status ep_combine_standard_moe(ep_handle* h, const void* expert_out, const float* weights,
+                                  const int32_t* indices, void* out, int32_t call_reset,
+                                  void* stream) {
+  (void)indices;
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->hasstd || h->state == kReady)
+    return fail(EP_ERR_STATE, "combine_standard_moe needs a packed layout");
+  if (!expert_out || !out) return fail(EP_ERR_INVALID_ARG, "expert_out and out must be non-NULL");
+  if (!aligned(expert_out, 16) || !aligned(out, 16))
+    return fail(EP_ERR_INVALID_ARG, "expert_out and out must be 16-byte aligned");
+  if (h->cfg.weighted_combine && !weights)
+    return fail(EP_ERR_INVALID_ARG, "weighted combine needs weights");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  const Geometry& g = h->g;
+  ep::CombineParams p;
+  memset(&p, 0, sizeof(p));
+  p.R = g.R; p.Tmax = g.Tmax; p.k = g.k; p.E_r = g.E_r; p.H = g.H;
+  for (int r = 0; r < g.R; ++r) p.ntok[r] = h->ntok[r];
+  p.cap = g.pcap;
+  p.segs_per_token = (g.H + ep::kCombineUnroll * 256 - 1) / (ep::kCombineUnroll * 256);
+  p.total_units = (int64_t)g.R * g.Tmax * p.segs_per_token;
+  p.weighted = h->cfg.weighted_combine != 0;
+  p.y = static_cast<const uint8_t*>(expert_out);
+  p.w = weights;
+  p.row_map = h->w.row_map;
+  p.out = static_cast<uint8_t*>(out);
+  cudaError_t e = ep::launch_combine_std(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
+                                         launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "standard-MoE combine launch");
+  h->state = kCombined;
+  if (call_reset) return ep_reset(h, stream);
+  return EP_OK;
+}
+
+ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
+                                     const int32_t* dispatch_indices, void* stream,
+                                     ep_std_moe_out* out) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->g.std_moe) return fail(EP_ERR_INVALID_ARG, "config has standard_moe = 0");
+  if (!h->has2d || h->state != kDispatched)
+    return fail(EP_ERR_STATE, "convert_dispatch_output needs a preceding dispatch");
+  if (!dispatch_x || !dispatch_indices)
+    return fail(EP_ERR_INVALID_ARG, "dispatch_x and dispatch_indices must be non-NULL");
+  if (!aligned(dispatch_x, 16)) return fail(EP_ERR_INVALID_ARG, "dispatch_x must be 16-byte aligned");
+  if (h->g.scale_row_bytes % 4 != 0)
+    return fail(EP_ERR_UNSUPPORTED, "convert needs scale rows that are a multiple of 4 bytes");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  const Geometry& g = h->g;
+  ep::ConvertParams p;
+  memset(&p, 0, sizeof(p));
+  p.R = g.R; p.Tmax = g.Tmax; p.k = g.k; p.E_r = g.E_r;
+  p.cap = g.cap; p.pcap = g.pcap;
+  p.cpr_recv = g.cpr_recv; p.nchunks = g.nchunks_recv;
+  p.H = g.H;
+  p.row_bytes = g.out_row_bytes;
+  p.scale_row_bytes = g.scale_row_bytes;
+  p.segs_per_row = (int)((g.out_row_bytes + ep::kCopyUnroll * 512 - 1) / (ep::kCopyUnroll * 512));
+  p.total_units = (int64_t)g.R * g.cap * p.segs_per_row;
+  p.recv_num_token = h->w.recv_num_token;
+  p.recv_idx = dispatch_indices;
+  p.src_pos = h->w.src_pos;
+  p.recv_x = static_cast<const uint8_t*>(dispatch_x);
+  p.recv_scales = h->w.recv_scales;
+  p.local16 = h->w.conv_local16;
+  p.chunk_cnt = h->w.conv_chunk_cnt;
+  p.chunk_off = h->w.conv_chunk_off;
+  p.expert_count = h->w.expert_count;
+  p.expert_offset = h->w.expert_offset;
+  p.rank_rows = h->w.rank_rows;
+  p.layout_range = h->w.layout_range;
+  p.packed_src_info = h->w.packed_src_info;
+  p.row_map = h->w.row_map;
+  p.packed_x = h->w.packed_x;
+  p.packed_scales = h->w.packed_scales;
+  p.ticket = h->w.tickets + 2;
+  p.err = h->w.err;
+  // row_map entries of dropped / foreign slots stay -1
+  cudaError_t e = cudaMemsetAsync(h->w.row_map, 0xFF, (size_t)g.R * g.Tmax * g.k * 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  e = ep::launch_convert_dispatch(p, g.scale_row_bytes > 0, launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "convert_dispatch_output launch");
+  h->hasstd = true;
+  if (out) {
+    out->packed_x = h->w.packed_x;
+    out->packed_scales = g.scale_row_bytes > 0 ? h->w.packed_scales : nullptr;
+    out->packed_count = h->w.expert_count;
+    out->packed_src_info = h->w.packed_src_info;
+    out->packed_layout_range = h->w.layout_range;
+    out->expert_offset = h->w.expert_offset;
+    out->rank_rows = h->w.rank_rows;
+    out->pcap = g.pcap;
+    out->x_row_bytes = g.out_row_bytes;
+  }
+  return EP_OK;
+}
+
+ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* combine_in,
+                                   void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->has2d || !h->hasstd || h->state == kReady)
+    return fail(EP_ERR_STATE, "convert_combine_input needs dispatch + convert_dispatch_output");
+  if (!packed_y || !combine_in) return fail(EP_ERR_INVALID_ARG, "NULL buffer");
+  if (!aligned(packed_y, 16) || !aligned(combine_in, 16))
+    return fail(EP_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  const Geometry& g = h->g;
+  ep::ConvertParams p;
+  memset(&p, 0, sizeof(p));
+  p.R = g.R; p.Tmax = g.Tmax; p.k = g.k; p.E_r = g.E_r;
+  p.cap = g.cap; p.pcap = g.pcap;
+  p.H = g.H;
+  p.segs_per_row = (g.H + ep::kCombineUnroll * 256 - 1) / (ep::kCombineUnroll * 256);
+  p.total_units = (int64_t)g.R * g.cap * p.segs_per_row;
+  p.recv_num_token = h->w.recv_num_token;
+  p.recv_idx = h->w.recv_idx;
+  p.src_pos = h->w.src_pos;
+  p.row_map = h->w.row_map;
+  p.packed_y = static_cast<const uint8_t*>(packed_y);
+  p.combine_in = static_cast<uint8_t*>(combine_in);
+  cudaError_t e = ep::launch_convert_combine(p, h->cfg.combine_dtype,
+                                             launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "convert_combine_input launch");
+  return EP_OK;
+}
+
+ep_status ep_sync(ep_handle* h, void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (h->needs_init) return EP_OK;
+  int32_t bits = 0;
+  e = cudaMemcpyAsync(&bits, h->w.err, sizeof(bits), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the error flags");
+  if (bits == 0) return EP_OK;
+  e = cudaMemsetAsync(h->w.err, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the error flags");
+  if (bits & (ep::kErrIndex | ep::kErrDuplicate))
+    return fail(EP_ERR_INVALID_INDEX, "an expert id was outside [-1, %d)%s", h->g.E,
+                (bits & ep::kErrDuplicate) ? " or repeated within a token (standard MoE)" : "");
+  return fail(EP_ERR_CAPACITY, "packed rows exceed max_packed_rows_per_rank = %lld",
+              (long long)h->g.pcap);
+}
+
+}  // extern "C"

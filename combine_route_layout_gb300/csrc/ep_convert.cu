@@ -1,0 +1,297 @@
+// Conversions between the 2D receive layout and the standard-MoE packed
+// layout (MORI-EP User Guide, section 4: convert_dispatch_output() and
+// convert_combine_input()).
+//
+// convert_dispatch_output: the receive rows of rank r are already in
+// (source rank, source token) order, so a row's place inside an expert
+// segment is its rank among the rank's receive rows with that expert. A
+// layout pass over chunks of 256 receive rows counts rows per local expert
+// with per-warp bitmaps, the last CTA scans the chunk counts and lays out the
+// 128-row padded segments, a copy pass moves the rows, and a final pass
+// derives each (expert, source rank) range by binary search over the sorted
+// src_info of the segment. The result equals dispatch_standard_moe().
+//
+// convert_combine_input: receive row i of rank r becomes the unweighted f32
+// sum of the token's packed rows on r (slots ascending), rounded once.
+#include "ep_kernels.cuh"
+
+namespace ep {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kWarps = kLayoutThreads / 32;
+
+__device__ bool elect_last(unsigned int* ticket) {
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (last) __threadfence();
+  return last;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertParams p) {
+  extern __shared__ uint32_t dyn[];
+  uint32_t* bits = dyn;                                         // [kWarps][E_r]
+  uint8_t* pre = reinterpret_cast<uint8_t*>(dyn + kWarps * p.E_r);  // [kWarps][E_r]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  const int r = c / p.cpr_recv;
+  const int64_t i = (int64_t)(c % p.cpr_recv) * kChunk + threadIdx.x;
+  const bool valid = i < __ldg(p.recv_num_token + r);
+  const int64_t row = (int64_t)r * p.cap + i;
+  const int E = p.R * p.E_r;
+
+  for (int q = threadIdx.x; q < kWarps * p.E_r; q += blockDim.x) bits[q] = 0u;
+  __syncthreads();
+  const uint32_t me = 1u << lane;
+  if (valid) {
+    for (int j = 0; j < p.k; ++j) {
+      const int e = __ldg(p.recv_idx + row * p.k + j);
+      uint16_t mark = 0xFFFFu;
+      if (e < -1 || e >= E) {
+        atomicOr(p.err, kErrIndex);
+      } else if (e >= 0 && e / p.E_r == r) {
+        const uint32_t old = atomicOr(&bits[warp * p.E_r + e % p.E_r], me);
+        if (old & me) atomicOr(p.err, kErrDuplicate);
+        else mark = 0;
+      }
+      p.local16[row * p.k + j] = mark;
+    }
+  }
+  __syncthreads();
+  for (int el = threadIdx.x; el < p.E_r; el += blockDim.x) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      pre[w * p.E_r + el] = (uint8_t)acc;
+      acc += __popc(bits[w * p.E_r + el]);
+    }
+    p.chunk_cnt[(int64_t)c * p.E_r + el] = acc;
+  }
+  __syncthreads();
+  if (valid) {
+    const uint32_t lt = lanemask_lt();
+    for (int j = 0; j < p.k; ++j) {
+      const int e = __ldg(p.recv_idx + row * p.k + j);
+      if (e < 0 || e >= E || e / p.E_r != r) continue;
+      if (p.local16[row * p.k + j] != 0u) continue;
+      const int el = e % p.E_r;
+      p.local16[row * p.k + j] =
+          (uint16_t)(pre[warp * p.E_r + el] + __popc(bits[warp * p.E_r + el] & lt));
+    }
+  }
+
+  if (!elect_last(p.ticket)) return;
+  for (int q = threadIdx.x; q < p.R * p.E_r; q += blockDim.x) {
+    const int rr = q / p.E_r, el = q % p.E_r;
+    int run = 0;
+    for (int cc = 0; cc < p.cpr_recv; ++cc) {
+      const int64_t ci = (int64_t)(rr * p.cpr_recv + cc) * p.E_r + el;
+      const int v = __ldcg(p.chunk_cnt + ci);
+      p.chunk_off[ci] = run;
+      run += v;
+    }
+    p.expert_count[q] = run;
+  }
+  __syncthreads();
+  for (int rr = threadIdx.x; rr < p.R; rr += blockDim.x) {
+    int64_t off = 0;
+    for (int el = 0; el < p.E_r; ++el) {
+      p.expert_offset[rr * p.E_r + el] = (int32_t)off;
+      const int64_t n = p.expert_count[rr * p.E_r + el];
+      off += (n + kPadRows - 1) / kPadRows * kPadRows;
+    }
+    p.rank_rows[rr] = (int32_t)off;
+    if (off > p.pcap) atomicOr(p.err, kErrCapacity);
+  }
+  __syncthreads();
+  for (int64_t q = threadIdx.x; q < (int64_t)p.R * p.E_r * kPadRows; q += blockDim.x) {
+    const int e = (int)(q / kPadRows), pad = (int)(q % kPadRows);
+    const int n = p.expert_count[e];
+    const int64_t prow = (int64_t)p.expert_offset[e] + n + pad;
+    const int64_t end = (int64_t)p.expert_offset[e] + (n + kPadRows - 1) / kPadRows * kPadRows;
+    if (prow < end && prow < p.pcap) p.packed_src_info[(int64_t)(e / p.E_r) * p.pcap + prow] = -1;
+  }
+  if (threadIdx.x == 0) *p.ticket = 0u;
+}
+
+template <bool SCALES>
+__global__ void __launch_bounds__(256) conv_copy_kernel(ConvertParams p) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.R * p.E_r;
+  const int64_t stride = (int64_t)p.R * p.Tmax;  // src_token_pos rank stride
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
+       u += nwarps) {
+    const int64_t rowg = u / p.segs_per_row;  // r * cap + i
+    const int seg = (int)(u - rowg * p.segs_per_row);
+    const int r = (int)(rowg / p.cap);
+    const int64_t i = rowg - (int64_t)r * p.cap;
+    if (i >= __ldg(p.recv_num_token + r)) continue;
+
+    const uint8_t* src = p.recv_x + rowg * p.row_bytes;
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int q = 0; q < kCopyUnroll; ++q) {
+      const int64_t off = ((int64_t)seg * kCopyUnroll + q) * 512 + lane * 16;
+      if (off < p.row_bytes) v[q] = ld_nc_v4(src + off);
+    }
+    int64_t my_row = -1;
+    if (lane < p.k) {
+      const int e = __ldg(p.recv_idx + rowg * p.k + lane);
+      const int l = __ldg(p.local16 + rowg * p.k + lane);
+      if (e >= 0 && e < E && e / p.E_r == r && l != 0xFFFF) {
+        const int el = e % p.E_r;
+        const int c = r * p.cpr_recv + (int)(i / kChunk);
+        const int64_t prow = (int64_t)__ldg(p.expert_offset + r * p.E_r + el) +
+                             __ldg(p.chunk_off + (int64_t)c * p.E_r + el) + l;
+        if (prow < p.pcap) my_row = (int64_t)r * p.pcap + prow;
+      }
+    }
+    const uint32_t vm = __ballot_sync(kFull, my_row >= 0);
+    if (seg == 0) {
+      const int pos = __ldg(p.src_pos + rowg);
+      const int64_t g = (pos / stride) * p.Tmax + pos % stride;
+      if (my_row >= 0) {
+        p.packed_src_info[my_row] = pos;
+        p.row_map[g * p.k + lane] = (int32_t)my_row;
+      }
+      if (SCALES) {
+        const int nw = p.scale_row_bytes >> 2;
+        const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(p.recv_scales + rowg * p.scale_row_bytes);
+        for (uint32_t mm = vm; mm; mm &= mm - 1) {
+          const int64_t pr = __shfl_sync(kFull, my_row, __ffs(mm) - 1);
+          uint32_t* sdst = reinterpret_cast<uint32_t*>(p.packed_scales + pr * p.scale_row_bytes);
+          for (int q = lane; q < nw; q += 32) sdst[q] = __ldg(ssrc + q);
+        }
+      }
+    }
+    for (uint32_t mm = vm; mm; mm &= mm - 1) {
+      const int64_t pr = __shfl_sync(kFull, my_row, __ffs(mm) - 1);
+      uint8_t* dst = p.packed_x + pr * p.row_bytes;
+#pragma unroll
+      for (int q = 0; q < kCopyUnroll; ++q) {
+        const int64_t off = ((int64_t)seg * kCopyUnroll + q) * 512 + lane * 16;
+        if (off < p.row_bytes) st_v4(dst + off, v[q]);
+      }
+    }
+  }
+}
+
+// layout_range[r][el][s] from the sorted src_info of each expert segment.
+__global__ void conv_range_kernel(ConvertParams p) {
+  const int64_t stride = (int64_t)p.R * p.Tmax;
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= (int64_t)p.R * p.E_r * p.R) return;
+  const int s = (int)(q % p.R);
+  const int e = (int)(q / p.R);  // r * E_r + el
+  const int r = e / p.E_r;
+  const int32_t* seg = p.packed_src_info + (int64_t)r * p.pcap + p.expert_offset[e];
+  const int n = p.expert_count[e];
+  auto lower = [&](int64_t key) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)seg[mid] < key) lo = mid + 1;
+      else hi = mid;
+    }
+    return lo;
+  };
+  const int b = lower((int64_t)s * stride), en = lower((int64_t)(s + 1) * stride);
+  p.layout_range[q] = (int64_t)(((uint64_t)(uint32_t)b << 32) | (uint32_t)(en - b));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) conv_combine_kernel(ConvertParams p) {
+  const int lane = threadIdx.x & 31;
+  constexpr int esz = DT == EP_DTYPE_BF16 ? 2 : 4;
+  const int64_t stride = (int64_t)p.R * p.Tmax;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
+       u += nwarps) {
+    const int64_t rowg = u / p.segs_per_row;
+    const int seg = (int)(u - rowg * p.segs_per_row);
+    const int r = (int)(rowg / p.cap);
+    const int64_t i = rowg - (int64_t)r * p.cap;
+    if (i >= __ldg(p.recv_num_token + r)) continue;
+    const int pos = __ldg(p.src_pos + rowg);
+    const int64_t g = (pos / stride) * p.Tmax + pos % stride;
+    int prow = -1;
+    if (lane < p.k) {
+      const int e = __ldg(p.recv_idx + rowg * p.k + lane);
+      if (e >= 0 && e / p.E_r == r) prow = __ldg(p.row_map + g * p.k + lane);
+    }
+    const uint32_t vm = __ballot_sync(kFull, prow >= 0);
+    for (int q = 0; q < kCombineUnroll; ++q) {
+      const int e0 = (seg * kCombineUnroll + q) * 256 + lane * 8;
+      const bool act = e0 < p.H;  // no early exit: the loop below shuffles
+      float acc[8];
+#pragma unroll
+      for (int z = 0; z < 8; ++z) acc[z] = 0.0f;
+      for (uint32_t mm = vm; mm; mm &= mm - 1) {
+        const int j = __ffs(mm) - 1;
+        const int pr = __shfl_sync(kFull, prow, j);
+        if (!act) continue;
+        const uint8_t* src = p.packed_y + (int64_t)pr * p.H * esz + (int64_t)e0 * esz;
+        float f[8];
+        if (DT == EP_DTYPE_BF16) {
+          const uint4 v = ld_nc_v4(src);
+          f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+          f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+        } else {
+          const uint4 a = ld_nc_v4(src), b = ld_nc_v4(src + 16);
+          f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+          f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+          f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y);
+          f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+        }
+#pragma unroll
+        for (int z = 0; z < 8; ++z) acc[z] = __fadd_rn(acc[z], f[z]);
+      }
+      if (!act) continue;
+      uint8_t* dst = p.combine_in + rowg * p.H * esz + (int64_t)e0 * esz;
+      if (DT == EP_DTYPE_BF16) {
+        st_v4(dst, make_uint4(cvt_bf16x2(acc[0], acc[1]), cvt_bf16x2(acc[2], acc[3]),
+                              cvt_bf16x2(acc[4], acc[5]), cvt_bf16x2(acc[6], acc[7])));
+      } else {
+        st_v4(dst, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                              __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+        st_v4(dst + 16, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                   __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
+                                    const LaunchCfg& lc, cudaStream_t st) {
+  if (p.nchunks == 0) return cudaSuccess;
+  const size_t smem = (size_t)kWarps * p.E_r * (sizeof(uint32_t) + 1);
+  conv_layout_kernel<<<p.nchunks, kLayoutThreads, smem, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.total_units > 0) {
+    auto k = with_scales ? conv_copy_kernel<true> : conv_copy_kernel<false>;
+    k<<<auto_grid(k, lc, p.total_units), lc.block, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t n = (int64_t)p.R * p.E_r * p.R;
+  conv_range_kernel<<<(int)((n + 255) / 256), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_combine(const ConvertParams& p, int dtype, const LaunchCfg& lc,
+                                   cudaStream_t st) {
+  if (p.total_units == 0) return cudaSuccess;
+  auto k = dtype == EP_DTYPE_BF16 ? conv_combine_kernel<EP_DTYPE_BF16>
+                                  : conv_combine_kernel<EP_DTYPE_FP32>;
+  k<<<auto_grid(k, lc, p.total_units), lc.block, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,274 @@
+// Dispatch payload movement (the second half of dispatch).
+//
+// MORI-EP User Guide, section 3, dispatch(): each received row carries the
+// token's payload, its weights and indices, and its scales. "Choosing an EP
+// API and backend" lists quantization as a dispatch feature and fixes the FP8
+// format to OCP E4M3; here the block is 128 elements with one f32 scale,
+// scale = amax / 448, codes = E4M3 round-to-nearest-even saturating of x/scale.
+//
+// Work is split into units of (token, column segment); each warp takes units
+// in a grid-stride loop, so all warps stay busy whatever the routing skew
+// (the unit count depends only on the source tokens). A unit loads its
+// segment of the source row once (16-byte non-coherent loads, all issued
+// before any dependent work) and writes it to every destination, so HBM sees
+// one read per token and one write per (token, destination). Segment 0 also
+// writes the per-row metadata. The destination slot is the chunk offset plus
+// the token's rank inside its chunk, both produced by the layout kernel.
+#include "ep_kernels.cuh"
+
+namespace ep {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Slot of this token on rank `lane` (2D layout), or -1.
+__device__ __forceinline__ int slot_on_lane_rank(const DispatchParams& p, int64_t g, int s, int t,
+                                                 uint32_t m, int lane) {
+  if (lane < p.R && ((m >> lane) & 1u)) {
+    const int c = s * p.cpr + t / kChunk;
+    return __ldg(p.chunk_off + (int64_t)c * p.R + lane) + (int)__ldg(p.local8 + g * p.R + lane);
+  }
+  return -1;
+}
+
+// Packed row (global index r*pcap + row) of slot `lane` (standard MoE), or -1.
+__device__ __forceinline__ int64_t row_on_lane_slot(const DispatchParams& p, int64_t g, int s,
+                                                    int t, int lane) {
+  if (lane >= p.k) return -1;
+  const int e = __ldg(p.idx + g * p.k + lane);
+  if (e < 0 || e >= p.E) return -1;
+  const int l = __ldg(p.local16 + g * p.k + lane);
+  if (l == 0xFFFF) return -1;
+  const int c = s * p.cpr + t / kChunk;
+  const int64_t row =
+      (int64_t)__ldg(p.expert_offset + e) + __ldg(p.chunk_off + (int64_t)c * p.E + e) + l;
+  if (row >= p.cap) return -1;  // capacity overflow is flagged by the layout kernel
+  return (int64_t)(e / p.E_r) * p.cap + row;
+}
+
+// Pass-through scale row of token g to receive row `row` (4-byte words when possible).
+__device__ __forceinline__ void copy_scale_row(const DispatchParams& p, int64_t g, int64_t row,
+                                               int lane) {
+  if ((p.scale_row_bytes & 3) == 0) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.scales_in + g * p.scale_row_bytes);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.out_scales + row * p.scale_row_bytes);
+    for (int i = lane; i < (p.scale_row_bytes >> 2); i += 32) dst[i] = __ldg(src + i);
+  } else {
+    const uint8_t* src = p.scales_in + g * p.scale_row_bytes;
+    uint8_t* dst = p.out_scales + row * p.scale_row_bytes;
+    for (int i = lane; i < p.scale_row_bytes; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+// Per-destination metadata of the 2D layout (segment 0 of a token only).
+__device__ void write_meta_2d(const DispatchParams& p, int64_t g, int s, int t, uint32_t m,
+                              int my_slot, int lane) {
+  if (lane < p.R) p.slot_map[g * p.R + lane] = my_slot;
+  if (my_slot >= 0) p.src_pos[(int64_t)lane * p.cap + my_slot] = s * (p.R * p.Tmax) + t;
+  const float wv = lane < p.k ? __ldg(p.w + g * p.k + lane) : 0.f;
+  const int iv = lane < p.k ? __ldg(p.idx + g * p.k + lane) : 0;
+  for (uint32_t mm = m; mm; mm &= mm - 1) {
+    const int r = __ffs(mm) - 1;
+    const int sl = __shfl_sync(kFull, my_slot, r);
+    const int64_t row = (int64_t)r * p.cap + sl;
+    if (lane < p.k) {
+      p.out_w[row * p.k + lane] = wv;
+      p.out_idx[row * p.k + lane] = iv;
+    }
+    if (p.scale_row_bytes > 0 && p.scales_in) copy_scale_row(p, g, row, lane);
+  }
+}
+
+// Per-slot metadata of the standard-MoE layout (segment 0 of a token only).
+__device__ void write_meta_std(const DispatchParams& p, int64_t g, int s, int t, int64_t my_row,
+                               int lane) {
+  if (lane < p.k) {
+    p.row_map[g * p.k + lane] = (int32_t)my_row;
+    if (my_row >= 0) p.src_pos[my_row] = s * (p.R * p.Tmax) + t;
+  }
+  if (p.scale_row_bytes > 0 && p.scales_in) {
+    for (uint32_t mm = __ballot_sync(kFull, my_row >= 0); mm; mm &= mm - 1) {
+      const int j = __ffs(mm) - 1;
+      copy_scale_row(p, g, __shfl_sync(kFull, my_row, j), lane);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ copy mode
+// Payload bits are moved unchanged: lane covers 16 bytes per 512-byte step.
+
+template <bool STD>
+__global__ void __launch_bounds__(256) dispatch_copy_kernel(DispatchParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
+       u += nwarps) {
+    const int64_t g = u / p.segs_per_token;
+    const int seg = (int)(u - g * p.segs_per_token);
+    const int s = (int)(g / p.Tmax), t = (int)(g - (int64_t)s * p.Tmax);
+    if (t >= p.ntok[s]) continue;
+
+    const uint8_t* src = p.x + g * p.in_row_bytes;
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int i = 0; i < kCopyUnroll; ++i) {
+      const int64_t off = ((int64_t)seg * kCopyUnroll + i) * 512 + lane * 16;
+      if (off < p.in_row_bytes) v[i] = ld_nc_v4(src + off);
+    }
+
+    if (!STD) {
+      const uint32_t m = __ldg(p.mask + g);
+      const int my_slot = slot_on_lane_rank(p, g, s, t, m, lane);
+      if (seg == 0) write_meta_2d(p, g, s, t, m, my_slot, lane);
+      for (uint32_t mm = m; mm; mm &= mm - 1) {
+        const int r = __ffs(mm) - 1;
+        const int sl = __shfl_sync(kFull, my_slot, r);
+        uint8_t* dst = p.out_x + ((int64_t)r * p.cap + sl) * p.out_row_bytes;
+#pragma unroll
+        for (int i = 0; i < kCopyUnroll; ++i) {
+          const int64_t off = ((int64_t)seg * kCopyUnroll + i) * 512 + lane * 16;
+          if (off < p.in_row_bytes) st_v4(dst + off, v[i]);
+        }
+      }
+    } else {
+      const int64_t my_row = row_on_lane_slot(p, g, s, t, lane);
+      if (seg == 0) write_meta_std(p, g, s, t, my_row, lane);
+      for (uint32_t mm = __ballot_sync(kFull, my_row >= 0); mm; mm &= mm - 1) {
+        const int j = __ffs(mm) - 1;
+        const int64_t row = __shfl_sync(kFull, my_row, j);
+        uint8_t* dst = p.out_x + row * p.out_row_bytes;
+#pragma unroll
+        for (int i = 0; i < kCopyUnroll; ++i) {
+          const int64_t off = ((int64_t)seg * kCopyUnroll + i) * 512 + lane * 16;
+          if (off < p.in_row_bytes) st_v4(dst + off, v[i]);
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ FP8 quant mode
+// bf16 in. Lane covers 16 consecutive elements (two 16-byte loads) per
+// 512-element step, so 8 lanes cover one 128-element block; the block's amax
+// is reduced with three xor-shuffles inside that 8-lane group.
+
+__device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q, float& scale) {
+  float f[16];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+  scale = __fdiv_rn(amax, 448.0f);
+  uint32_t c[8];
+  if (amax == 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = cvt_e4m3x2(f[2 * i], f[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+  }
+  q.x = c[0] | (c[1] << 16);
+  q.y = c[2] | (c[3] << 16);
+  q.z = c[4] | (c[5] << 16);
+  q.w = c[6] | (c[7] << 16);
+}
+
+template <bool STD>
+__global__ void __launch_bounds__(256) dispatch_quant_kernel(DispatchParams p) {
+  const int lane = threadIdx.x & 31;
+  const int nb = p.H / 128;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
+       u += nwarps) {
+    const int64_t g = u / p.segs_per_token;
+    const int seg = (int)(u - g * p.segs_per_token);
+    const int s = (int)(g / p.Tmax), t = (int)(g - (int64_t)s * p.Tmax);
+    if (t >= p.ntok[s]) continue;
+
+    const uint8_t* src = p.x + g * p.in_row_bytes;
+    uint4 a[kQuantUnroll], b[kQuantUnroll];
+#pragma unroll
+    for (int i = 0; i < kQuantUnroll; ++i) {
+      const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
+      if (e0 < p.H) {
+        a[i] = ld_nc_v4(src + (int64_t)e0 * 2);
+        b[i] = ld_nc_v4(src + (int64_t)e0 * 2 + 16);
+      } else {
+        a[i] = make_uint4(0, 0, 0, 0);
+        b[i] = a[i];
+      }
+    }
+    uint4 q[kQuantUnroll];
+    float sc[kQuantUnroll];
+#pragma unroll
+    for (int i = 0; i < kQuantUnroll; ++i) quant16(a[i], b[i], q[i], sc[i]);
+
+    // Each destination row gets the codes and the block scales.
+    auto put = [&](int64_t row) {
+      uint8_t* dst = p.out_x + row * p.out_row_bytes;
+      float* dsc = reinterpret_cast<float*>(p.out_scales) + row * nb;
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
+        if (e0 < p.H) {
+          st_v4(dst + e0, q[i]);
+          if ((lane & 7) == 0) dsc[e0 / 128] = sc[i];
+        }
+      }
+    };
+    if (!STD) {
+      const uint32_t m = __ldg(p.mask + g);
+      const int my_slot = slot_on_lane_rank(p, g, s, t, m, lane);
+      if (seg == 0) write_meta_2d(p, g, s, t, m, my_slot, lane);
+      for (uint32_t mm = m; mm; mm &= mm - 1) {
+        const int r = __ffs(mm) - 1;
+        const int sl = __shfl_sync(kFull, my_slot, r);
+        put((int64_t)r * p.cap + sl);
+      }
+    } else {
+      const int64_t my_row = row_on_lane_slot(p, g, s, t, lane);
+      if (seg == 0) write_meta_std(p, g, s, t, my_row, lane);
+      for (uint32_t mm = __ballot_sync(kFull, my_row >= 0); mm; mm &= mm - 1) {
+        const int j = __ffs(mm) - 1;
+        put(__shfl_sync(kFull, my_row, j));
+      }
+    }
+  }
+}
+
+template <bool STD>
+cudaError_t launch_dispatch(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+                            cudaStream_t st) {
+  if (p.total_units == 0) return cudaSuccess;
+  if (quant) {
+    auto k = dispatch_quant_kernel<STD>;
+    k<<<auto_grid(k, lc, p.total_units), lc.block, 0, st>>>(p);
+  } else {
+    auto k = dispatch_copy_kernel<STD>;
+    k<<<auto_grid(k, lc, p.total_units), lc.block, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_2d(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+                               cudaStream_t st) {
+  return launch_dispatch<false>(p, quant, lc, st);
+}
+
+cudaError_t launch_dispatch_std(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+                                cudaStream_t st) {
+  return launch_dispatch<true>(p, quant, lc, st);
+}
+
+}  // namespace ep

@@ -1,0 +1,230 @@
+// Internal declarations shared by the libep translation units: kernel
+// parameter blocks, launch helpers and small device primitives written as
+// inline PTX for sm_103a.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+constexpr int kChunk = 256;          // source tokens per routing-layout CTA
+constexpr int kLayoutThreads = 256;  // one thread per token of the chunk
+constexpr int kPadRows = 128;        // standard-MoE segment alignment
+
+// Device error bits, reported by ep_sync.
+constexpr int kErrIndex = 1;      // expert id outside [-1, E)
+constexpr int kErrDuplicate = 2;  // repeated expert id in one token (standard MoE)
+constexpr int kErrCapacity = 4;   // packed rows beyond max_packed_rows_per_rank
+
+// ------------------------------------------------------------ parameter blocks
+
+struct LayoutParams {
+  int R, Tmax, k, E_r, E;
+  int cpr;        // chunks per source rank = ceil(Tmax / kChunk)
+  int nchunks;    // R * cpr
+  int ntok[EP_MAX_WORLD_SIZE];
+  const int32_t* idx;         // [R][Tmax][k]
+  // 2D layout
+  uint32_t* mask;             // [R*Tmax] destination-rank bitmask
+  uint8_t* local8;            // [R*Tmax][R] rank of the token among the chunk's tokens sent to r
+  int32_t* recv_num_token;    // [R]
+  // standard-MoE layout
+  uint16_t* local16;          // [R*Tmax][k] rank among the chunk's rows of that expert; 0xFFFF = none
+  int32_t* expert_count;      // [E]
+  int32_t* expert_offset;     // [E] segment start within its rank
+  int32_t* rank_rows;         // [R]
+  int64_t* layout_range;      // [R][E_r][R]
+  int32_t* packed_src_info;   // [R][pcap]
+  int64_t pcap;
+  // shared
+  int32_t* chunk_cnt;         // [nchunks][R] (2D) or [nchunks][E] (standard MoE)
+  int32_t* chunk_off;         // exclusive prefix over chunks, same shape
+  unsigned int* ticket;       // last-CTA election counter (returns to 0)
+  int32_t* err;
+};
+
+struct DispatchParams {
+  int R, Tmax, k, E_r, E, cpr;
+  int ntok[EP_MAX_WORLD_SIZE];
+  int64_t cap;                 // receive rows per rank (2D) or pcap (standard MoE)
+  int H;
+  int64_t in_row_bytes;        // bytes of one source payload row
+  int64_t out_row_bytes;       // bytes of one received payload row
+  int scale_row_bytes;         // pass-through scale bytes per row (copy mode)
+  int segs_per_token;          // work units per token
+  int64_t total_units;
+  const uint8_t* x;
+  const float* w;
+  const int32_t* idx;
+  const uint8_t* scales_in;
+  // layout (from the routing-layout kernel)
+  const uint32_t* mask;
+  const uint8_t* local8;
+  const uint16_t* local16;
+  const int32_t* chunk_off;
+  const int32_t* expert_offset;
+  // outputs
+  int32_t* slot_map;           // 2D: [R*Tmax][R]
+  int32_t* src_pos;            // 2D: [R][cap]; standard MoE: packed_src_info [R][pcap]
+  int32_t* row_map;            // standard MoE: [R*Tmax][k] global packed row
+  uint8_t* out_x;
+  uint8_t* out_scales;         // [rows][H/128] f32 (quant) or [rows][scale_row_bytes]
+  float* out_w;                // 2D only
+  int32_t* out_idx;            // 2D only
+};
+
+struct CombineParams {
+  int R, Tmax, k, E_r, H;
+  int ntok[EP_MAX_WORLD_SIZE];
+  int64_t cap;                 // rows per rank of the expert-output buffer
+  int segs_per_token;
+  int64_t total_units;
+  int weighted;
+  const uint8_t* y;
+  const float* w;              // 2D: receive-layout weights; standard MoE: source weights
+  const int32_t* recv_idx;     // 2D: receive-layout expert ids (owner test for weights)
+  const int32_t* idx;          // standard MoE: source expert ids
+  const int32_t* slot_map;     // 2D
+  const int32_t* row_map;      // standard MoE
+  uint8_t* out;
+  float* out_w;
+};
+
+struct ConvertParams {
+  int R, Tmax, k, E_r;
+  int64_t cap, pcap;
+  int cpr_recv;                // chunks per rank over the receive capacity
+  int nchunks;
+  int H;
+  int64_t row_bytes;
+  int scale_row_bytes;
+  int segs_per_row;
+  int64_t total_units;
+  const int32_t* recv_num_token;
+  const int32_t* recv_idx;     // [R][cap][k]
+  const int32_t* src_pos;      // [R][cap]
+  const uint8_t* recv_x;
+  const uint8_t* recv_scales;
+  uint16_t* local16;           // [R][cap][k]
+  int32_t* chunk_cnt;          // [nchunks][E_r]
+  int32_t* chunk_off;
+  int32_t* expert_count;       // [R][E_r]
+  int32_t* expert_offset;
+  int32_t* rank_rows;
+  int64_t* layout_range;
+  int32_t* packed_src_info;
+  int32_t* row_map;            // [R*Tmax][k]
+  uint8_t* packed_x;
+  uint8_t* packed_scales;
+  unsigned int* ticket;
+  int32_t* err;
+  // convert_combine_input
+  const uint8_t* packed_y;
+  uint8_t* combine_in;
+};
+
+// ------------------------------------------------------------------ launchers
+// Each returns the cudaError_t of its launch.
+
+struct LaunchCfg {
+  int grid_hint;  // CTAs requested by the caller; <= 0: one full wave
+  int block;      // threads per CTA (multiple of 32, <= 256)
+  int sm_count;
+};
+
+// CTAs for a grid-stride kernel over `units` warp-sized work units: the
+// caller's request, else as many CTAs as fit on the GPU at once, never more
+// than the units need.
+template <typename Kernel>
+inline int auto_grid(Kernel kernel, const LaunchCfg& lc, int64_t units, size_t smem = 0) {
+  const int64_t warps = lc.block / 32;
+  const int64_t need = (units + warps - 1) / warps;
+  int64_t grid = lc.grid_hint;
+  if (grid <= 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, lc.block, smem) !=
+            cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    grid = (int64_t)lc.sm_count * per_sm;
+  }
+  if (grid > need) grid = need;
+  return grid < 1 ? 1 : (int)grid;
+}
+
+cudaError_t launch_layout_2d(const LayoutParams& p, cudaStream_t st);
+cudaError_t launch_layout_std(const LayoutParams& p, cudaStream_t st);
+cudaError_t launch_dispatch_2d(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+                               cudaStream_t st);
+cudaError_t launch_dispatch_std(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+                                cudaStream_t st);
+cudaError_t launch_combine_2d(const CombineParams& p, int in_dtype, int out_dtype,
+                              const LaunchCfg& lc, cudaStream_t st);
+cudaError_t launch_combine_std(const CombineParams& p, int in_dtype, int out_dtype,
+                               const LaunchCfg& lc, cudaStream_t st);
+cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
+                                    const LaunchCfg& lc, cudaStream_t st);
+cudaError_t launch_convert_combine(const ConvertParams& p, int dtype, const LaunchCfg& lc,
+                                   cudaStream_t st);
+
+// Work-unit geometry used by the launchers and the host library alike.
+constexpr int kCopyUnroll = 4;       // 16-byte vectors per lane per copy unit
+constexpr int kQuantUnroll = 2;      // 512-element steps per quantisation unit
+constexpr int kCombineUnroll = 2;    // 256-element steps per combine unit
+
+}  // namespace ep
+
+// ---------------------------------------------------------------- device PTX
+#ifdef __CUDACC__
+namespace ep {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Two f32 -> two OCP E4M3 codes, round to nearest even, saturating to +-448.
+// Returns lo in bits 0..7 and hi in bits 8..15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two f32 -> two bf16 (round to nearest even); lo in bits 0..15.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace ep
+#endif

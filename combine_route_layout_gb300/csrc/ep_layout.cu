@@ -1,0 +1,250 @@
+// Routing layout (the first half of dispatch).
+//
+// MORI-EP User Guide, section 3, dispatch(): each token goes to the ranks that
+// own its top-k experts (owner = expert / num_experts_per_rank, section 2),
+// once per distinct rank (MORI issue 57: "reduce redundant data transfer"),
+// and dispatch reports recv_num_token. Receive rows are ordered by
+// (source rank, source token), which makes every result deterministic.
+//
+// One CTA handles a chunk of 256 consecutive tokens of one source rank, one
+// thread per token. It computes the token's destination set, the chunk's
+// per-destination counts (warp ballots) and each token's rank inside the
+// chunk, and stores them. The last CTA to finish (elected with one atomic
+// ticket after a release fence; no CTA ever waits on another) scans the
+// per-chunk counts into per-chunk offsets. The dispatch kernel adds the two.
+//
+// The standard-MoE variant (User Guide, section 4) counts rows per expert
+// instead of per rank (no deduplication), using per-warp expert bitmaps in
+// shared memory, and the last CTA also lays out the 128-row padded expert
+// segments and the per-source-rank layout ranges.
+#include "ep_kernels.cuh"
+
+namespace ep {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kWarps = kLayoutThreads / 32;
+
+// Exclusive scan of one int per thread across the CTA; *total gets the sum.
+__device__ int cta_exclusive_scan(int v, int* sm, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    sm[lane] = w;
+  }
+  __syncthreads();
+  const int before = warp ? sm[warp - 1] : 0;
+  *total = sm[nw - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+// Release this CTA's global writes and report whether it finished last.
+__device__ bool elect_last_cta(unsigned int* ticket) {
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (last) __threadfence();
+  return last;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads) layout_2d_kernel(LayoutParams p) {
+  __shared__ int wcnt[kWarps][EP_MAX_WORLD_SIZE];
+  __shared__ int wpre[kWarps][EP_MAX_WORLD_SIZE];
+  __shared__ int scan_sm[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  const int s = c / p.cpr;
+  const int t = (c % p.cpr) * kChunk + threadIdx.x;
+  const bool valid = t < p.ntok[s];
+  const int64_t g = (int64_t)s * p.Tmax + t;
+
+  uint32_t m = 0;
+  if (valid) {
+    const int32_t* row = p.idx + g * p.k;
+    for (int j = 0; j < p.k; ++j) {
+      const int e = __ldg(row + j);
+      if (e == -1) continue;
+      if (e < -1 || e >= p.E) {
+        atomicOr(p.err, kErrIndex);
+        continue;
+      }
+      m |= 1u << (e / p.E_r);
+    }
+    p.mask[g] = m;
+  }
+  for (int r = 0; r < p.R; ++r) {
+    const uint32_t b = __ballot_sync(kFull, (m >> r) & 1u);
+    if (lane == 0) wcnt[warp][r] = __popc(b);
+  }
+  __syncthreads();
+  if (threadIdx.x < p.R) {
+    const int r = threadIdx.x;
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      wpre[w][r] = acc;
+      acc += wcnt[w][r];
+    }
+    p.chunk_cnt[(int64_t)c * p.R + r] = acc;
+  }
+  __syncthreads();
+  const uint32_t lt = lanemask_lt();
+  for (int r = 0; r < p.R; ++r) {
+    const uint32_t b = __ballot_sync(kFull, (m >> r) & 1u);
+    if ((m >> r) & 1u) p.local8[g * p.R + r] = (uint8_t)(wpre[warp][r] + __popc(b & lt));
+  }
+
+  if (!elect_last_cta(p.ticket)) return;
+  // Last CTA: per destination rank, exclusive scan of the chunk counts.
+  const int per = (p.nchunks + blockDim.x - 1) / blockDim.x;
+  const int c0 = threadIdx.x * per;
+  const int c1 = min(c0 + per, p.nchunks);
+  for (int r = 0; r < p.R; ++r) {
+    int sum = 0;
+    for (int cc = c0; cc < c1; ++cc) sum += __ldcg(p.chunk_cnt + (int64_t)cc * p.R + r);
+    int total;
+    int ex = cta_exclusive_scan(sum, scan_sm, &total);
+    for (int cc = c0; cc < c1; ++cc) {
+      const int v = __ldcg(p.chunk_cnt + (int64_t)cc * p.R + r);
+      p.chunk_off[(int64_t)cc * p.R + r] = ex;
+      ex += v;
+    }
+    if (threadIdx.x == 0) p.recv_num_token[r] = total;
+  }
+  if (threadIdx.x == 0) *p.ticket = 0u;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams p) {
+  // bits[w][e]: lanes of warp w whose token selects expert e; pre[w][e]: rows of
+  // expert e from warps before w in this chunk.
+  extern __shared__ uint32_t dyn[];
+  uint32_t* bits = dyn;
+  uint8_t* pre = reinterpret_cast<uint8_t*>(dyn + kWarps * p.E);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  const int s = c / p.cpr;
+  const int t = (c % p.cpr) * kChunk + threadIdx.x;
+  const bool valid = t < p.ntok[s];
+  const int64_t g = (int64_t)s * p.Tmax + t;
+
+  for (int i = threadIdx.x; i < kWarps * p.E; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  const uint32_t me = 1u << lane;
+  if (valid) {
+    const int32_t* row = p.idx + g * p.k;
+    for (int j = 0; j < p.k; ++j) {
+      const int e = __ldg(row + j);
+      uint16_t mark = 0xFFFFu;
+      if (e < -1 || e >= p.E) {
+        atomicOr(p.err, kErrIndex);
+      } else if (e >= 0) {
+        const uint32_t old = atomicOr(&bits[warp * p.E + e], me);
+        if (old & me) atomicOr(p.err, kErrDuplicate);  // repeated id: later slot dropped
+        else mark = 0;
+      }
+      p.local16[g * p.k + j] = mark;  // 0 = counted (filled in below), 0xFFFF = no row
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      pre[w * p.E + e] = (uint8_t)acc;
+      acc += __popc(bits[w * p.E + e]);
+    }
+    p.chunk_cnt[(int64_t)c * p.E + e] = acc;
+  }
+  __syncthreads();
+  if (valid) {
+    const uint32_t lt = lanemask_lt();
+    const int32_t* row = p.idx + g * p.k;
+    for (int j = 0; j < p.k; ++j) {
+      const int e = __ldg(row + j);
+      if (e < 0 || e >= p.E) continue;
+      if (p.local16[g * p.k + j] != 0u) continue;  // duplicate already marked
+      p.local16[g * p.k + j] =
+          (uint16_t)(pre[warp * p.E + e] + __popc(bits[warp * p.E + e] & lt));
+    }
+  }
+
+  if (!elect_last_cta(p.ticket)) return;
+  // Last CTA: per expert, scan over chunks (grouped by source rank), then the
+  // padded segment offsets per destination rank and the padding rows.
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    const int r = e / p.E_r, el = e % p.E_r;
+    int run = 0;
+    for (int src = 0; src < p.R; ++src) {
+      const int begin = run;
+      for (int cc = 0; cc < p.cpr; ++cc) {
+        const int64_t ci = (int64_t)(src * p.cpr + cc) * p.E + e;
+        const int v = __ldcg(p.chunk_cnt + ci);
+        p.chunk_off[ci] = run;
+        run += v;
+      }
+      p.layout_range[((int64_t)r * p.E_r + el) * p.R + src] =
+          (int64_t)(((uint64_t)(uint32_t)begin << 32) | (uint32_t)(run - begin));
+    }
+    p.expert_count[e] = run;
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
+    int64_t off = 0;
+    for (int el = 0; el < p.E_r; ++el) {
+      p.expert_offset[r * p.E_r + el] = (int32_t)off;
+      const int64_t n = p.expert_count[r * p.E_r + el];
+      off += (n + kPadRows - 1) / kPadRows * kPadRows;
+    }
+    p.rank_rows[r] = (int32_t)off;
+    if (off > p.pcap) atomicOr(p.err, kErrCapacity);
+  }
+  __syncthreads();
+  // padding rows carry src_info = -1
+  for (int64_t i = threadIdx.x; i < (int64_t)p.E * kPadRows; i += blockDim.x) {
+    const int e = (int)(i / kPadRows), q = (int)(i % kPadRows);
+    const int n = p.expert_count[e];
+    const int64_t row = (int64_t)p.expert_offset[e] + n + q;
+    const int64_t end = (int64_t)p.expert_offset[e] + (n + kPadRows - 1) / kPadRows * kPadRows;
+    if (row < end && row < p.pcap) p.packed_src_info[(int64_t)(e / p.E_r) * p.pcap + row] = -1;
+  }
+  if (threadIdx.x == 0) *p.ticket = 0u;
+}
+
+}  // namespace
+
+cudaError_t launch_layout_2d(const LayoutParams& p, cudaStream_t st) {
+  if (p.nchunks == 0) return cudaSuccess;
+  layout_2d_kernel<<<p.nchunks, kLayoutThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layout_std(const LayoutParams& p, cudaStream_t st) {
+  if (p.nchunks == 0) return cudaSuccess;
+  const size_t smem = (size_t)kWarps * p.E * (sizeof(uint32_t) + 1);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(layout_std_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  layout_std_kernel<<<p.nchunks, kLayoutThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,361 @@
+"""Thin Python binding of libep (include/ep.h).
+
+Argument marshalling only: every step of dispatch and combine runs in the
+CUDA kernels of libep.so. Functions named ep_* wrap the C entry points one
+to one (pointers as ints); EpDispatchCombineOp mirrors the operator API of
+the MORI-EP User Guide (section 3 "Operator API", section 4 "Standard MoE
+Compatibility") on torch tensors, with PyTorch used only for device memory
+and streams. There is no CPU fallback: importing this module fails if the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, fields
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libep.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = -1
+EP_ERR_STATE = -2
+EP_ERR_CAPACITY = -3
+EP_ERR_INVALID_INDEX = -4
+EP_ERR_CUDA = -5
+EP_ERR_WORKSPACE = -7
+EP_ERR_UNSUPPORTED = -8
+
+EP_DTYPE_BF16 = 0
+EP_DTYPE_FP32 = 1
+EP_DTYPE_FP8_E4M3 = 2
+EP_QUANT_NONE = 0
+EP_QUANT_FP8_E4M3_BLOCK128 = 1
+
+_TORCH_OF = {EP_DTYPE_BF16: torch.bfloat16, EP_DTYPE_FP32: torch.float32,
+             EP_DTYPE_FP8_E4M3: torch.float8_e4m3fn}
+_EP_OF = {v: k for k, v in _TORCH_OF.items()}
+
+
+class EpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libep status {status}: {message}")
+        self.status = status
+
+
+class ep_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "world_size", "hidden_dim", "scale_dim", "scale_type_size", "max_token_type_size",
+        "max_num_inp_token_per_rank", "num_experts_per_rank", "num_experts_per_token",
+        "data_type", "quant_type", "combine_dtype", "combine_out_dtype", "weighted_combine",
+        "standard_moe", "max_packed_rows_per_rank", "block_num", "warp_num_per_block")]
+
+
+class ep_dispatch_out(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("weights", ctypes.c_void_p), ("indices", ctypes.c_void_p),
+                ("recv_num_token", ctypes.c_void_p), ("src_token_pos", ctypes.c_void_p),
+                ("cap", ctypes.c_int64), ("x_row_bytes", ctypes.c_int64),
+                ("scale_row_bytes", ctypes.c_int64)]
+
+
+class ep_std_moe_out(ctypes.Structure):
+    _fields_ = [("packed_x", ctypes.c_void_p), ("packed_scales", ctypes.c_void_p),
+                ("packed_count", ctypes.c_void_p), ("packed_src_info", ctypes.c_void_p),
+                ("packed_layout_range", ctypes.c_void_p), ("expert_offset", ctypes.c_void_p),
+                ("rank_rows", ctypes.c_void_p), ("pcap", ctypes.c_int64),
+                ("x_row_bytes", ctypes.c_int64)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                          "(there is no fallback path)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    S = ctypes.c_int
+    sig = {
+        "ep_workspace_size": (Z, [P]),
+        "ep_config_create": (S, [P, P, Z, P]),
+        "ep_destroy": (None, [P]),
+        "ep_dispatch": (S, [P, P, P, P, P, P, P, P]),
+        "ep_combine": (S, [P, P, P, P, P, P, I, P]),
+        "ep_get_dispatch_src_token_pos": (S, [P, P]),
+        "ep_reset": (S, [P, P]),
+        "ep_dispatch_standard_moe": (S, [P, P, P, P, P, P, P, P]),
+        "ep_combine_standard_moe": (S, [P, P, P, P, P, I, P]),
+        "ep_convert_dispatch_output": (S, [P, P, P, P, P]),
+        "ep_convert_combine_input": (S, [P, P, P, P]),
+        "ep_sync": (S, [P, P]),
+        "ep_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int) -> None:
+    if status != EP_OK:
+        raise EpError(status, _lib.ep_last_error().decode())
+
+
+def _ref(obj):
+    return ctypes.byref(obj) if obj is not None else None
+
+
+# ------------------------------------------------------- C entry points
+
+def ep_workspace_size(cfg: ep_config) -> int:
+    return int(_lib.ep_workspace_size(ctypes.byref(cfg)))
+
+
+def ep_config_create(cfg: ep_config, d_workspace: int, workspace_bytes: int) -> int:
+    h = ctypes.c_void_p()
+    _check(_lib.ep_config_create(ctypes.byref(cfg), d_workspace, workspace_bytes, ctypes.byref(h)))
+    return h.value
+
+
+def ep_destroy(handle: int) -> None:
+    _lib.ep_destroy(handle)
+
+
+def ep_dispatch(handle, x, weights, scales, indices, num_tokens, stream) -> ep_dispatch_out:
+    out = ep_dispatch_out()
+    nt = (ctypes.c_int32 * len(num_tokens))(*[int(n) for n in num_tokens])
+    _check(_lib.ep_dispatch(handle, x, weights, scales, indices, nt, stream, ctypes.byref(out)))
+    return out
+
+
+def ep_combine(handle, expert_out, weights, indices, out, out_weights, call_reset, stream) -> None:
+    _check(_lib.ep_combine(handle, expert_out, weights, indices, out, out_weights,
+                           int(call_reset), stream))
+
+
+def ep_get_dispatch_src_token_pos(handle) -> int:
+    p = ctypes.c_void_p()
+    _check(_lib.ep_get_dispatch_src_token_pos(handle, ctypes.byref(p)))
+    return p.value
+
+
+def ep_reset(handle, stream=None) -> None:
+    _check(_lib.ep_reset(handle, stream))
+
+
+def ep_dispatch_standard_moe(handle, x, weights, scales, indices, num_tokens,
+                             stream) -> ep_std_moe_out:
+    out = ep_std_moe_out()
+    nt = (ctypes.c_int32 * len(num_tokens))(*[int(n) for n in num_tokens])
+    _check(_lib.ep_dispatch_standard_moe(handle, x, weights, scales, indices, nt, stream,
+                                         ctypes.byref(out)))
+    return out
+
+
+def ep_combine_standard_moe(handle, expert_out, weights, indices, out, call_reset, stream) -> None:
+    _check(_lib.ep_combine_standard_moe(handle, expert_out, weights, indices, out,
+                                        int(call_reset), stream))
+
+
+def ep_convert_dispatch_output(handle, dispatch_x, dispatch_indices, stream) -> ep_std_moe_out:
+    out = ep_std_moe_out()
+    _check(_lib.ep_convert_dispatch_output(handle, dispatch_x, dispatch_indices, stream,
+                                           ctypes.byref(out)))
+    return out
+
+
+def ep_convert_combine_input(handle, packed_y, combine_in, stream) -> None:
+    _check(_lib.ep_convert_combine_input(handle, packed_y, combine_in, stream))
+
+
+def ep_sync(handle, stream) -> None:
+    _check(_lib.ep_sync(handle, stream))
+
+
+def ep_last_error() -> str:
+    return _lib.ep_last_error().decode()
+
+
+# ------------------------------------------------------- operator class
+
+@dataclass
+class EpDispatchCombineConfig:
+    """EpDispatchCombineConfig (MORI-EP User Guide, section 2) for simulated
+    ranks: all world_size ranks live in this process, so `rank` is absent."""
+    data_type: torch.dtype
+    world_size: int
+    hidden_dim: int
+    scale_dim: int
+    scale_type_size: int
+    max_token_type_size: int
+    max_num_inp_token_per_rank: int
+    num_experts_per_rank: int
+    num_experts_per_token: int
+    warp_num_per_block: int = 8
+    block_num: int = -1
+    quant_type: str = "none"            # "none" | "fp8_e4m3_block128"
+    combine_dtype: torch.dtype = torch.bfloat16
+    combine_out_dtype: torch.dtype = torch.bfloat16
+    weighted_combine: bool = False
+    standard_moe: bool = False
+    max_packed_rows_per_rank: int = 0
+
+    def to_c(self) -> ep_config:
+        c = ep_config()
+        for f in fields(self):
+            v = getattr(self, f.name)
+            if f.name in ("data_type", "combine_dtype", "combine_out_dtype"):
+                v = _EP_OF[v]
+            elif f.name == "quant_type":
+                v = {"none": EP_QUANT_NONE, "fp8_e4m3_block128": EP_QUANT_FP8_E4M3_BLOCK128}[v]
+            setattr(c, f.name, int(v))
+        return c
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+class EpDispatchCombineOp:
+    """Operator over one workspace (User Guide, section 3). Inputs carry all
+    ranks: x [R, Tmax, H], weights [R, Tmax, k], indices [R, Tmax, k] int32;
+    num_tokens gives each source rank's token count (default Tmax)."""
+
+    def __init__(self, config: EpDispatchCombineConfig, device: torch.device | str = "cuda"):
+        self.config = config
+        self.c = config.to_c()
+        nbytes = ep_workspace_size(self.c)
+        if nbytes == 0:
+            raise EpError(EP_ERR_INVALID_ARG, ep_last_error())
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self._handle = ep_config_create(self.c, self.workspace.data_ptr(), nbytes)
+        R, T = config.world_size, config.max_num_inp_token_per_rank
+        self.cap = R * T
+
+    def __del__(self):
+        h = getattr(self, "_handle", None)
+        if h:
+            ep_destroy(h)
+            self._handle = None
+
+    # views into the workspace ------------------------------------------------
+    def _view(self, ptr: int, dtype: torch.dtype, shape) -> torch.Tensor:
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        off = ptr - self.workspace.data_ptr()
+        assert 0 <= off and off + nbytes <= self.workspace.numel()
+        return self.workspace[off:off + nbytes].view(dtype).view(*shape)
+
+    def _num_tokens(self, num_tokens):
+        R, T = self.config.world_size, self.config.max_num_inp_token_per_rank
+        return [T] * R if num_tokens is None else [int(n) for n in num_tokens]
+
+    @property
+    def _dispatch_dtype(self):
+        return torch.float8_e4m3fn if self.config.quant_type != "none" else self.config.data_type
+
+    @staticmethod
+    def decode_send_flat_idx(pos: int, world_size: int, max_tokens: int) -> tuple[int, int]:
+        return divmod(int(pos), world_size * max_tokens)
+
+    # section 3 ----------------------------------------------------------------
+    def dispatch(self, input, weights, scales, indices, num_tokens=None):
+        cfg = self.config
+        R, H, k = cfg.world_size, cfg.hidden_dim, cfg.num_experts_per_token
+        o = ep_dispatch(self._handle, _ptr(input), _ptr(weights), _ptr(scales), _ptr(indices),
+                        self._num_tokens(num_tokens), _stream())
+        x = self._view(o.x, self._dispatch_dtype, (R, self.cap, H))
+        if o.scales:
+            if cfg.quant_type != "none":
+                sc = self._view(o.scales, torch.float32, (R, self.cap, H // 128))
+            else:
+                sc = self._view(o.scales, torch.uint8, (R, self.cap, o.scale_row_bytes))
+        else:
+            sc = None
+        w = self._view(o.weights, torch.float32, (R, self.cap, k))
+        idx = self._view(o.indices, torch.int32, (R, self.cap, k))
+        recv = self._view(o.recv_num_token, torch.int32, (R,))
+        return x, w, sc, idx, recv
+
+    def combine(self, input, weights, indices, out=None, out_weights=None, call_reset=False,
+                want_weights=True):
+        cfg = self.config
+        R, T, H, k = (cfg.world_size, cfg.max_num_inp_token_per_rank, cfg.hidden_dim,
+                      cfg.num_experts_per_token)
+        if out is None:
+            out = torch.empty((R, T, H), dtype=cfg.combine_out_dtype, device=input.device)
+        if out_weights is None and want_weights and weights is not None:
+            out_weights = torch.empty((R, T, k), dtype=torch.float32, device=input.device)
+        ep_combine(self._handle, _ptr(input), _ptr(weights), _ptr(indices), _ptr(out),
+                   _ptr(out_weights), call_reset, _stream())
+        return out, out_weights
+
+    def reset(self):
+        ep_reset(self._handle, _stream())
+
+    def get_dispatch_src_token_pos(self):
+        p = ep_get_dispatch_src_token_pos(self._handle)
+        return self._view(p, torch.int32, (self.config.world_size, self.cap))
+
+    def sync(self):
+        ep_sync(self._handle, _stream())
+
+    # section 4 ----------------------------------------------------------------
+    def _std_views(self, o: ep_std_moe_out):
+        cfg = self.config
+        R, Er, H = cfg.world_size, cfg.num_experts_per_rank, cfg.hidden_dim
+        return {
+            "packed_recv_x": self._view(o.packed_x, self._dispatch_dtype, (R, o.pcap, H)),
+            "packed_recv_scales": (self._view(o.packed_scales, torch.float32, (R, o.pcap, H // 128))
+                                   if o.packed_scales and cfg.quant_type != "none" else None),
+            "packed_recv_count": self._view(o.packed_count, torch.int32, (R, Er)),
+            "packed_recv_src_info": self._view(o.packed_src_info, torch.int32, (R, o.pcap)),
+            "packed_recv_layout_range": self._view(o.packed_layout_range, torch.int64, (R, Er, R)),
+            "expert_offset": self._view(o.expert_offset, torch.int32, (R, Er)),
+            "rank_rows": self._view(o.rank_rows, torch.int32, (R,)),
+        }
+
+    def dispatch_standard_moe(self, input, weights, scales, indices, num_tokens=None):
+        o = ep_dispatch_standard_moe(self._handle, _ptr(input), _ptr(weights), _ptr(scales),
+                                     _ptr(indices), self._num_tokens(num_tokens), _stream())
+        self.pcap = o.pcap
+        return self._std_views(o)
+
+    def combine_standard_moe(self, input, weights, indices, out=None, call_reset=False):
+        cfg = self.config
+        R, T, H = cfg.world_size, cfg.max_num_inp_token_per_rank, cfg.hidden_dim
+        if out is None:
+            out = torch.empty((R, T, H), dtype=cfg.combine_out_dtype, device=input.device)
+        ep_combine_standard_moe(self._handle, _ptr(input), _ptr(weights), _ptr(indices),
+                                _ptr(out), call_reset, _stream())
+        return out
+
+    def convert_dispatch_output(self, dispatch_out_x, dispatch_out_topk_idx):
+        o = ep_convert_dispatch_output(self._handle, _ptr(dispatch_out_x),
+                                       _ptr(dispatch_out_topk_idx), _stream())
+        self.pcap = o.pcap
+        v = self._std_views(o)
+        return (v["packed_recv_x"], v["packed_recv_count"], v["packed_recv_src_info"],
+                v["packed_recv_layout_range"])
+
+    def convert_combine_input(self, packed_recv_x, packed_recv_src_info=None,
+                              packed_recv_layout_range=None, out=None):
+        """The src_info / layout_range arguments are accepted for API parity;
+        the handle's packed layout defines where each row goes."""
+        cfg = self.config
+        if out is None:
+            out = torch.empty((cfg.world_size, self.cap, cfg.hidden_dim), dtype=cfg.combine_dtype,
+                              device=packed_recv_x.device)
+        ep_convert_combine_input(self._handle, _ptr(packed_recv_x), _ptr(out), _stream())
+        return out

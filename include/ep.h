@@ -1,0 +1,257 @@
+/*
+ * libep -- MoE expert-parallel dispatch / combine on one GB300 (sm_103a).
+ *
+ * C ABI. All pointers named d_* or documented as "device" are CUDA device
+ * pointers; everything else is host memory. `stream` is a cudaStream_t passed
+ * as void* (NULL = legacy default stream). No function allocates device
+ * memory: the caller hands one device workspace to ep_config_create and owns
+ * every input and combine output; dispatch outputs are views into that
+ * workspace, valid until the next ep_dispatch*, ep_reset or ep_destroy.
+ * Dispatch and combine never synchronise the host, so they can be captured
+ * into a CUDA graph.
+ *
+ * The EP ranks are simulated: rank r's receive buffers are partitions of the
+ * workspace, and inputs carry all ranks at once as [world_size][...] arrays.
+ *
+ * Operation definitions come from the MORI-EP User Guide:
+ *   section 2 "Configuration" (EpDispatchCombineConfig fields),
+ *   section 3 "Operator API" (dispatch(), combine(), reset(),
+ *             get_dispatch_src_token_pos()),
+ *   section 4 "Standard MoE Compatibility (DeepEP)" (dispatch_standard_moe(),
+ *             combine_standard_moe(), convert_dispatch_output(),
+ *             convert_combine_input()),
+ * and from "Choosing an EP API and backend" (EP paths table: gather combine
+ * in BF16/FP32, quantization; restrictions: OCP E4M3 FP8).
+ *
+ * Thread safety: a handle is not thread-safe; distinct handles are
+ * independent. Errors: every call returns an ep_status; ep_last_error()
+ * gives a message for the calling thread's most recent failure.
+ */
+#ifndef EP_H_
+#define EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EP_MAX_WORLD_SIZE 32   /* simulated ranks per handle */
+#define EP_MAX_TOPK 32         /* num_experts_per_token */
+#define EP_MAX_EXPERTS 1024    /* world_size * num_experts_per_rank */
+#define EP_QUANT_BLOCK 128     /* FP8 block: one f32 scale per 128 elements */
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = -1,    /* bad config, pointer, size or alignment */
+    EP_ERR_STATE = -2,          /* call out of order (e.g. combine before dispatch) */
+    EP_ERR_CAPACITY = -3,       /* packed standard-MoE rows exceed the configured capacity */
+    EP_ERR_INVALID_INDEX = -4,  /* expert id outside [-1, E) (or duplicated, standard MoE) */
+    EP_ERR_CUDA = -5,           /* a CUDA runtime call failed; see ep_last_error() */
+    EP_ERR_WORKSPACE = -7,      /* workspace NULL, misaligned or too small */
+    EP_ERR_UNSUPPORTED = -8     /* valid request this build does not implement */
+} ep_status;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,
+    EP_DTYPE_FP32 = 1,
+    EP_DTYPE_FP8_E4M3 = 2       /* OCP E4M3 (bias 7, max 448, NaN = S.1111.111) */
+} ep_dtype;
+
+typedef enum {
+    EP_QUANT_NONE = 0,          /* dispatch moves the input bits unchanged */
+    EP_QUANT_FP8_E4M3_BLOCK128 = 1  /* bf16 in; E4M3 codes + one f32 scale per 128 elements out */
+} ep_quant;
+
+/*
+ * Mirrors EpDispatchCombineConfig (User Guide, section 2). `rank` is absent:
+ * all world_size ranks live in this process. Additions are marked (+).
+ */
+typedef struct ep_config {
+    int32_t world_size;                  /* simulated EP ranks, 1..EP_MAX_WORLD_SIZE */
+    int32_t hidden_dim;                  /* H, elements per token */
+    int32_t scale_dim;                   /* pass-through scales per token (0 = none); with
+                                            FP8 quantisation 0 or H/128 (then 4-byte) */
+    int32_t scale_type_size;             /* bytes per pass-through scale element */
+    int32_t max_token_type_size;         /* bytes of the widest combine element (2 or 4) */
+    int32_t max_num_inp_token_per_rank;  /* Tmax */
+    int32_t num_experts_per_rank;        /* E_r; expert e is owned by rank e / E_r */
+    int32_t num_experts_per_token;       /* k (top-k), 1..EP_MAX_TOPK */
+    int32_t data_type;                   /* ep_dtype of dispatch input tokens: BF16, FP32 or
+                                            FP8_E4M3 (pre-quantised pass-through) */
+    int32_t quant_type;                  /* (+) ep_quant; FP8 block quant needs BF16 input and
+                                            H % 128 == 0 */
+    int32_t combine_dtype;               /* (+) ep_dtype of expert outputs given to combine:
+                                            BF16 or FP32 */
+    int32_t combine_out_dtype;           /* (+) ep_dtype of combine output: BF16 or FP32 */
+    int32_t weighted_combine;            /* (+) 0: plain sum over ranks; 1: weighted sum */
+    int32_t standard_moe;                /* (+) 1: reserve the per-expert packed layout */
+    int32_t max_packed_rows_per_rank;    /* (+) packed rows per rank; 0 = worst case
+                                            R*Tmax*min(k,E_r) + 127*E_r */
+    int32_t block_num;                   /* CTAs per launch; <= 0: one wave sized to the GPU */
+    int32_t warp_num_per_block;          /* warps per CTA; <= 0: 8 */
+} ep_config;
+
+typedef struct ep_handle ep_handle;
+
+/*
+ * Dispatch results (User Guide, section 3, dispatch() return values). All
+ * pointers are device views into the workspace. cap = world_size * Tmax rows
+ * per destination rank; rank r's rows start at r * cap. Only the first
+ * recv_num_token[r] rows of rank r are written.
+ */
+typedef struct ep_dispatch_out {
+    void* x;                    /* [R][cap][H] payload: input dtype, or E4M3 codes */
+    void* scales;               /* [R][cap][scale_row_bytes]; NULL when there are none */
+    float* weights;             /* [R][cap][k] router weights of the received token */
+    int32_t* indices;           /* [R][cap][k] global expert ids of the token (-1 kept) */
+    int32_t* recv_num_token;    /* [R] rows received by each rank (device) */
+    int32_t* src_token_pos;     /* [R][cap] src_rank * (R * Tmax) + src_token_id */
+    int64_t cap;                /* rows per destination rank */
+    int64_t x_row_bytes;        /* bytes per payload row */
+    int64_t scale_row_bytes;    /* bytes per scale row (0 = none) */
+} ep_dispatch_out;
+
+/*
+ * Standard-MoE (DeepEP-style) packed layout (User Guide, section 4). Rank r
+ * holds one contiguous segment per local expert, in ascending expert order,
+ * each padded to a multiple of 128 rows; rows inside a segment are ordered
+ * by (source rank, source token). Rank r's rows start at r * pcap.
+ */
+typedef struct ep_std_moe_out {
+    void* packed_x;                 /* [R][pcap][H] payload */
+    void* packed_scales;            /* [R][pcap][H/128] f32 with FP8 quantisation, else NULL */
+    int32_t* packed_count;          /* [R][E_r] rows per local expert */
+    int32_t* packed_src_info;       /* [R][pcap] src_token_pos encoding; -1 on padding rows */
+    int64_t* packed_layout_range;   /* [R][E_r][R] (begin << 32) | count per source rank,
+                                       begin relative to the expert segment */
+    int32_t* expert_offset;         /* [R][E_r] first row of each expert segment */
+    int32_t* rank_rows;             /* [R] padded rows in use on each rank */
+    int64_t pcap;                   /* rows reserved per rank */
+    int64_t x_row_bytes;
+} ep_std_moe_out;
+
+/* Workspace bytes needed by `cfg` (0 if the config is invalid). Host only. */
+size_t ep_workspace_size(const ep_config* cfg);
+
+/*
+ * Validate `cfg` and carve `d_workspace` (device, 256-byte aligned, at least
+ * ep_workspace_size bytes, owned by the caller for the handle's lifetime).
+ * Makes no CUDA call; the first dispatch clears the workspace's counters on
+ * its stream. Returns EP_ERR_INVALID_ARG / EP_ERR_WORKSPACE on bad input.
+ */
+ep_status ep_config_create(const ep_config* cfg, void* d_workspace, size_t workspace_bytes,
+                           ep_handle** out_handle);
+
+/* Free the host-side handle (the workspace stays the caller's). NULL is a no-op. */
+void ep_destroy(ep_handle* h);
+
+/*
+ * dispatch() (User Guide, section 3): route every source token once to each
+ * distinct rank owning one of its top-k experts (owner = id / E_r; -1 slots
+ * are dropped) and copy its payload, weights, indices and scales there.
+ *   x          device [R][Tmax][H], data_type; 16-byte aligned
+ *   weights    device [R][Tmax][k] f32
+ *   scales     device [R][Tmax][scale_dim * scale_type_size bytes] or NULL
+ *              (must be NULL with FP8 block quantisation, which computes them)
+ *   indices    device [R][Tmax][k] int32 in [-1, R*E_r)
+ *   num_tokens host [R], tokens held by each source rank, each <= Tmax
+ * Receive rows are ordered by (source rank, source token). State must be
+ * READY; afterwards it is DISPATCHED. An out-of-range expert id is skipped
+ * and raises EP_ERR_INVALID_INDEX at the next ep_sync.
+ */
+ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const void* scales,
+                      const int32_t* indices, const int32_t* num_tokens, void* stream,
+                      ep_dispatch_out* out);
+
+/*
+ * combine() (User Guide, section 3; gather combine): for each source token,
+ * sum the expert-output rows of its copies in ascending destination-rank
+ * order in an f32 accumulator starting at +0, weighted by the rank's slot
+ * weights when weighted_combine, and round once to combine_out_dtype.
+ *   expert_out   device [R][cap][H] combine_dtype, rows in dispatch order
+ *   weights      device [R][cap][k] f32 in receive layout (dispatch's weights
+ *                output or the caller's), or NULL (then out_weights must be
+ *                NULL and weighted_combine 0)
+ *   indices      accepted for API parity; the dispatch layout is used
+ *   out          device [R][Tmax][H] combine_out_dtype (rows past num_tokens untouched)
+ *   out_weights  device [R][Tmax][k] f32 or NULL: the weight row of the copy on
+ *                the lowest destination rank (zeros for a token sent nowhere)
+ *   call_reset   nonzero: ep_reset after the combine
+ * State must be DISPATCHED or COMBINED (2D layout present).
+ */
+ep_status ep_combine(ep_handle* h, const void* expert_out, const float* weights,
+                     const int32_t* indices, void* out, float* out_weights, int32_t call_reset,
+                     void* stream);
+
+/* get_dispatch_src_token_pos() (User Guide, section 3): device [R][cap]. */
+ep_status ep_get_dispatch_src_token_pos(ep_handle* h, const int32_t** d_src_token_pos);
+
+/* reset() (User Guide, section 3): back to READY; invalidates dispatch views.
+ * Enqueues nothing on `stream`. */
+ep_status ep_reset(ep_handle* h, void* stream);
+
+/*
+ * dispatch_standard_moe() (User Guide, section 4): routing and copy into
+ * the packed per-expert layout in one pass (one row per valid (token, slot),
+ * no per-rank deduplication). Same inputs as ep_dispatch. Needs
+ * standard_moe = 1. Capacity overflow raises EP_ERR_CAPACITY at ep_sync and
+ * the overflowing rows are not written.
+ */
+ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* weights,
+                                   const void* scales, const int32_t* indices,
+                                   const int32_t* num_tokens, void* stream, ep_std_moe_out* out);
+
+/*
+ * combine_standard_moe() (User Guide, section 4): per source token, over its
+ * valid slots in (owner rank, slot) order, acc = fmaf(w, y, acc) (weighted)
+ * or acc + y, f32 from +0, rounded once to combine_out_dtype.
+ *   expert_out  device [R][pcap][H] combine_dtype, packed layout
+ *   weights     device [R][Tmax][k] f32 source-side router weights (NULL if unweighted)
+ *   indices     accepted for API parity; the packed layout is used
+ *   out         device [R][Tmax][H]
+ * Needs a packed layout (ep_dispatch_standard_moe or ep_convert_dispatch_output).
+ */
+ep_status ep_combine_standard_moe(ep_handle* h, const void* expert_out, const float* weights,
+                                  const int32_t* indices, void* out, int32_t call_reset,
+                                  void* stream);
+
+/*
+ * convert_dispatch_output() (User Guide, section 4): build the packed layout
+ * from the 2D receive buffers of the preceding ep_dispatch.
+ *   dispatch_x        device [R][cap][H] (normally ep_dispatch_out.x)
+ *   dispatch_indices  device [R][cap][k] (normally ep_dispatch_out.indices)
+ * The result equals ep_dispatch_standard_moe on the same inputs. FP8 scales
+ * are carried along when the dispatch quantised.
+ */
+ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
+                                     const int32_t* dispatch_indices, void* stream,
+                                     ep_std_moe_out* out);
+
+/*
+ * convert_combine_input() (User Guide, section 4): from packed expert
+ * outputs, build the 2D combine input: receive row i of rank r gets the
+ * unweighted f32 sum, over the token's slots owned by r in ascending slot
+ * order, of their packed rows, rounded once to combine_dtype.
+ *   packed_y    device [R][pcap][H] combine_dtype
+ *   combine_in  device [R][cap][H] combine_dtype (rows past recv_num_token untouched)
+ * Needs both layouts (ep_dispatch, then ep_convert_dispatch_output).
+ */
+ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* combine_in,
+                                   void* stream);
+
+/*
+ * (+) Wait for `stream`, then report and clear device-detected errors
+ * (EP_ERR_INVALID_INDEX, EP_ERR_CAPACITY) raised by earlier launches.
+ */
+ep_status ep_sync(ep_handle* h, void* stream);
+
+/* (+) Message for the calling thread's last failed call ("" if none). */
+const char* ep_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H_ */

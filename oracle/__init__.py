@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_route.argtypes = [I, I, I, I, P, P, P, P, P]
         _lib.oracle_place_rows.argtypes = [I, I, L, P, P, P, P]
         _lib.oracle_combine.argtypes = [I, I, I, I, I, P, P, P, I, P, P, I, I, P, P]
+        _lib.oracle_combine_tokens.argtypes = [I, I, I, I, I, P, L, P, P, I, P, P, I, I, P, P]
+        _lib.oracle_std_combine_tokens.argtypes = [I, I, I, I, P, L, P, P, I, P, P, I, I, P]
         _lib.oracle_std_layout.argtypes = [I, I, I, I, L, P, P, P, P, P, P, P, P]
         _lib.oracle_std_place_rows.argtypes = [I, I, I, L, P, P, P, P]
         _lib.oracle_std_combine.argtypes = [I, I, I, I, I, P, P, P, I, P, P, I, I, P]
@@ -196,6 +198,28 @@ def combine(y: np.ndarray, idx: np.ndarray, ntok: np.ndarray, slot: np.ndarray,
     return out, out_w
 
 
+def combine_tokens(tokens: np.ndarray, y: np.ndarray, idx: np.ndarray, slot: np.ndarray,
+                   experts_per_rank: int, w_recv: np.ndarray | None = None,
+                   weighted: bool = False, out_dtype: str = "bf16"):
+    """Combine for the listed global source tokens g = s*Tmax + t only:
+    returns (out [n, H], out_w [n, k] or None)."""
+    tokens = np.ascontiguousarray(tokens, np.int64)
+    y = np.ascontiguousarray(y)
+    R, cap, H = y.shape
+    T = cap // R
+    k = idx.shape[-1]
+    od = _dt(out_dtype)
+    out = np.zeros((len(tokens), H), np.uint16 if od == DT_BF16 else np.float32)
+    out_w = np.zeros((len(tokens), k), np.float32) if w_recv is not None else None
+    wr = None if w_recv is None else np.ascontiguousarray(w_recv, np.float32)
+    _check(lib().oracle_combine_tokens(R, T, k, experts_per_rank, H, _p(tokens), len(tokens),
+                                       _p(np.ascontiguousarray(idx, np.int32)),
+                                       _p(np.ascontiguousarray(slot, np.int32)), _dt(y.dtype.type),
+                                       _p(y), _p(wr), int(weighted), od, _p(out), _p(out_w)),
+           "combine_tokens")
+    return out, out_w
+
+
 # --------------------------------------------------------- standard MoE
 
 def std_layout(idx: np.ndarray, ntok: np.ndarray, experts_per_rank: int, pcap: int):
@@ -256,6 +280,25 @@ def std_combine(Y: np.ndarray, idx: np.ndarray, ntok: np.ndarray, row_map: np.nd
                                     _p(np.ascontiguousarray(row_map, np.int32)),
                                     _dt(Y.dtype.type), _p(Y), _p(wp), int(weighted), od, _p(out)),
            "std_combine")
+    return out
+
+
+def std_combine_tokens(tokens: np.ndarray, Y: np.ndarray, idx: np.ndarray, row_map: np.ndarray,
+                       experts_per_rank: int, w: np.ndarray | None = None,
+                       weighted: bool = True, out_dtype: str = "fp32") -> np.ndarray:
+    tokens = np.ascontiguousarray(tokens, np.int64)
+    Y = np.ascontiguousarray(Y)
+    R = idx.shape[0]
+    k = idx.shape[-1]
+    H = Y.shape[-1]
+    od = _dt(out_dtype)
+    out = np.zeros((len(tokens), H), np.uint16 if od == DT_BF16 else np.float32)
+    wp = None if w is None else np.ascontiguousarray(w, np.float32)
+    _check(lib().oracle_std_combine_tokens(R, k, experts_per_rank, H, _p(tokens), len(tokens),
+                                           _p(np.ascontiguousarray(idx, np.int32)),
+                                           _p(np.ascontiguousarray(row_map, np.int32)),
+                                           _dt(Y.dtype.type), _p(Y), _p(wp), int(weighted), od,
+                                           _p(out)), "std_combine_tokens")
     return out
 
 

@@ -224,45 +224,74 @@ void oracle_place_rows(int R, int Tmax, int64_t row_bytes, const int32_t* ntok,
  * [Back] gather combine in BF16/FP32. y is [R][R*Tmax][H] (y_dtype),
  * w_recv [R][R*Tmax][k] or NULL, out [R][Tmax][H] (out_dtype),
  * out_w [R][Tmax][k] or NULL. Readings R5, R6. */
+/* One source token g = s*Tmax + t of the 2D combine; out_row [H], out_w_row [k] or NULL. */
+static void combine_token(int R, int Tmax, int k, int E_r, int H, int64_t g, const int32_t* idx,
+                          const int32_t* slot, int y_dtype, const void* y, const float* w_recv,
+                          int weighted, int out_dtype, void* out_row, float* out_w_row) {
+    int64_t cap = (int64_t)R * Tmax;
+    float wr[ORC_MAX_RANKS];
+    for (int r = 0; r < R; ++r) {
+        wr[r] = 0.0f;
+        int32_t i = slot[g * R + r];
+        if (i < 0 || !w_recv) continue;
+        for (int j = 0; j < k; ++j) {
+            int32_t e = idx[g * k + j];
+            if (e >= 0 && e / E_r == r) wr[r] = wr[r] + w_recv[((int64_t)r * cap + i) * k + j];
+        }
+    }
+    if (out_w_row) {
+        int rmin = -1;
+        for (int r = R - 1; r >= 0; --r)
+            if (slot[g * R + r] >= 0) rmin = r;
+        for (int j = 0; j < k; ++j)
+            out_w_row[j] = (rmin >= 0 && w_recv)
+                ? w_recv[((int64_t)rmin * cap + slot[g * R + rmin]) * k + j] : 0.0f;
+    }
+    for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int r = 0; r < R; ++r) {
+            int32_t i = slot[g * R + r];
+            if (i < 0) continue;
+            float v = load_elem(y_dtype, y, ((int64_t)r * cap + i) * H + h);
+            if (weighted) acc = fmaf(wr[r], v, acc);
+            else acc = acc + v;
+        }
+        store_elem(out_dtype, out_row, h, acc);
+    }
+}
+
+static int64_t dtype_bytes(int dt) { return dt == DT_BF16 ? 2 : 4; }
+
+/* [Guide] s.3 combine(): gather expert outputs back to the source token;
+ * [Back] gather combine in BF16/FP32. y is [R][R*Tmax][H] (y_dtype),
+ * w_recv [R][R*Tmax][k] or NULL, out [R][Tmax][H] (out_dtype),
+ * out_w [R][Tmax][k] or NULL. Readings R5, R6. */
 int oracle_combine(int R, int Tmax, int k, int E_r, int H, const int32_t* ntok,
                    const int32_t* idx, const int32_t* slot, int y_dtype, const void* y,
                    const float* w_recv, int weighted, int out_dtype, void* out, float* out_w) {
     if (R < 1 || R > ORC_MAX_RANKS) return ORC_ERR_ARG;
     if (weighted && !w_recv) return ORC_ERR_ARG;
-    int64_t cap = (int64_t)R * Tmax;
     for (int s = 0; s < R; ++s)
         for (int t = 0; t < ntok[s]; ++t) {
             int64_t g = (int64_t)s * Tmax + t;
-            float wr[ORC_MAX_RANKS];
-            for (int r = 0; r < R; ++r) {
-                wr[r] = 0.0f;
-                int32_t i = slot[g * R + r];
-                if (i < 0 || !w_recv) continue;
-                for (int j = 0; j < k; ++j) {
-                    int32_t e = idx[g * k + j];
-                    if (e >= 0 && e / E_r == r) wr[r] = wr[r] + w_recv[((int64_t)r * cap + i) * k + j];
-                }
-            }
-            if (out_w) {
-                int rmin = -1;
-                for (int r = R - 1; r >= 0; --r)
-                    if (slot[g * R + r] >= 0) rmin = r;
-                for (int j = 0; j < k; ++j)
-                    out_w[g * k + j] = (rmin >= 0 && w_recv)
-                        ? w_recv[((int64_t)rmin * cap + slot[g * R + rmin]) * k + j] : 0.0f;
-            }
-            for (int h = 0; h < H; ++h) {
-                float acc = 0.0f;
-                for (int r = 0; r < R; ++r) {
-                    int32_t i = slot[g * R + r];
-                    if (i < 0) continue;
-                    float v = load_elem(y_dtype, y, ((int64_t)r * cap + i) * H + h);
-                    if (weighted) acc = fmaf(wr[r], v, acc);
-                    else acc = acc + v;
-                }
-                store_elem(out_dtype, out, g * H + h, acc);
-            }
+            combine_token(R, Tmax, k, E_r, H, g, idx, slot, y_dtype, y, w_recv, weighted,
+                          out_dtype, (uint8_t*)out + g * H * dtype_bytes(out_dtype),
+                          out_w ? out_w + g * k : NULL);
         }
+    return ORC_OK;
+}
+
+/* The same combine for a list of source tokens g only: out [n][H], out_w [n][k]. */
+int oracle_combine_tokens(int R, int Tmax, int k, int E_r, int H, const int64_t* tokens,
+                          int64_t n, const int32_t* idx, const int32_t* slot, int y_dtype,
+                          const void* y, const float* w_recv, int weighted, int out_dtype,
+                          void* out, float* out_w) {
+    if (R < 1 || R > ORC_MAX_RANKS) return ORC_ERR_ARG;
+    if (weighted && !w_recv) return ORC_ERR_ARG;
+    for (int64_t q = 0; q < n; ++q)
+        combine_token(R, Tmax, k, E_r, H, tokens[q], idx, slot, y_dtype, y, w_recv, weighted,
+                      out_dtype, (uint8_t*)out + q * H * dtype_bytes(out_dtype),
+                      out_w ? out_w + q * k : NULL);
     return ORC_OK;
 }
 
@@ -336,6 +365,24 @@ void oracle_std_place_rows(int R, int Tmax, int k, int64_t row_bytes, const int3
         }
 }
 
+/* One source token of the standard-MoE combine; out_row [H]. */
+static void std_combine_token(int R, int k, int E_r, int H, int64_t g, const int32_t* idx,
+                              const int32_t* row_map, int y_dtype, const void* Y, const float* w,
+                              int weighted, int out_dtype, void* out_row) {
+    for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int r = 0; r < R; ++r)
+            for (int j = 0; j < k; ++j) {
+                int32_t e = idx[g * k + j];
+                if (e < 0 || e / E_r != r) continue;
+                float v = load_elem(y_dtype, Y, (int64_t)row_map[g * k + j] * H + h);
+                if (weighted) acc = fmaf(w[g * k + j], v, acc);
+                else acc = acc + v;
+            }
+        store_elem(out_dtype, out_row, h, acc);
+    }
+}
+
 /* [Guide] s.4 combine_standard_moe(), reading R8. Y is the packed expert
  * output [R][pcap][H]; w [R][Tmax][k] source-side router weights. */
 int oracle_std_combine(int R, int Tmax, int k, int E_r, int H, const int32_t* ntok,
@@ -346,19 +393,22 @@ int oracle_std_combine(int R, int Tmax, int k, int E_r, int H, const int32_t* nt
     for (int s = 0; s < R; ++s)
         for (int t = 0; t < ntok[s]; ++t) {
             int64_t g = (int64_t)s * Tmax + t;
-            for (int h = 0; h < H; ++h) {
-                float acc = 0.0f;
-                for (int r = 0; r < R; ++r)
-                    for (int j = 0; j < k; ++j) {
-                        int32_t e = idx[g * k + j];
-                        if (e < 0 || e / E_r != r) continue;
-                        float v = load_elem(y_dtype, Y, (int64_t)row_map[g * k + j] * H + h);
-                        if (weighted) acc = fmaf(w[g * k + j], v, acc);
-                        else acc = acc + v;
-                    }
-                store_elem(out_dtype, out, g * H + h, acc);
-            }
+            std_combine_token(R, k, E_r, H, g, idx, row_map, y_dtype, Y, w, weighted, out_dtype,
+                              (uint8_t*)out + g * H * dtype_bytes(out_dtype));
         }
+    return ORC_OK;
+}
+
+/* The same for a list of source tokens g only: out [n][H]. */
+int oracle_std_combine_tokens(int R, int k, int E_r, int H, const int64_t* tokens, int64_t n,
+                              const int32_t* idx, const int32_t* row_map, int y_dtype,
+                              const void* Y, const float* w, int weighted, int out_dtype,
+                              void* out) {
+    if (R < 1 || R > ORC_MAX_RANKS) return ORC_ERR_ARG;
+    if (weighted && !w) return ORC_ERR_ARG;
+    for (int64_t q = 0; q < n; ++q)
+        std_combine_token(R, k, E_r, H, tokens[q], idx, row_map, y_dtype, Y, w, weighted,
+                          out_dtype, (uint8_t*)out + q * H * dtype_bytes(out_dtype));
     return ORC_OK;
 }
 

@@ -1,0 +1,136 @@
+"""The C ABI library without a GPU: every symbol declared in include/ep.h is
+exported, and the host-side validation, workspace sizing and state machine
+answer without touching a device (no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep.h")
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_route_layout_gb300.build import build
+    build()
+    from combine_route_layout_gb300 import ep as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(ep):
+    names = declared_functions()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(ep.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_multicast_anywhere():
+    """No TMA multicast form is used in any source of the product."""
+    for d, _, files in os.walk(os.path.join(ROOT, "combine_route_layout_gb300")):
+        for f in files:
+            if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+                assert "multicast" not in open(os.path.join(d, f)).read(), f
+
+
+def cfg(ep, **kw):
+    base = dict(world_size=8, hidden_dim=7168, scale_dim=0, scale_type_size=4,
+                max_token_type_size=4, max_num_inp_token_per_rank=4096, num_experts_per_rank=32,
+                num_experts_per_token=8, data_type=ep.EP_DTYPE_BF16,
+                quant_type=ep.EP_QUANT_FP8_E4M3_BLOCK128, combine_dtype=ep.EP_DTYPE_BF16,
+                combine_out_dtype=ep.EP_DTYPE_BF16, weighted_combine=0, standard_moe=0,
+                max_packed_rows_per_rank=0, block_num=0, warp_num_per_block=0)
+    base.update(kw)
+    c = ep.ep_config()
+    for k, v in base.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_workspace_size_grows_with_layouts(ep):
+    a = ep.ep_workspace_size(cfg(ep))
+    b = ep.ep_workspace_size(cfg(ep, standard_moe=1))
+    # 2D receive payload alone: 8 ranks x 32768 rows x 7168 FP8 bytes
+    assert a >= 8 * 32768 * 7168
+    assert b > a + 8 * (32768 * 8 + 127 * 32) * 7168 - 1
+
+
+@pytest.mark.parametrize("bad", [dict(world_size=0), dict(world_size=33), dict(hidden_dim=100),
+                                 dict(num_experts_per_token=0), dict(num_experts_per_token=33),
+                                 dict(num_experts_per_rank=0), dict(num_experts_per_rank=200),
+                                 dict(max_num_inp_token_per_rank=0), dict(data_type=9),
+                                 dict(hidden_dim=200), dict(quant_type=5),
+                                 dict(combine_out_dtype=2), dict(scale_dim=3),
+                                 dict(data_type=1, quant_type=1), dict(warp_num_per_block=16)])
+def test_invalid_configs_rejected(ep, bad):
+    c = cfg(ep, **bad)
+    assert ep.ep_workspace_size(c) == 0
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_config_create(c, 1 << 20, 1 << 40)
+    assert ei.value.status == ep.EP_ERR_INVALID_ARG
+
+
+FAKE = 1 << 40   # an aligned address that is never dereferenced by these tests
+
+
+def small(ep, **kw):
+    return cfg(ep, hidden_dim=256, max_num_inp_token_per_rank=16, num_experts_per_rank=4,
+               num_experts_per_token=4, quant_type=0, **kw)
+
+
+def test_workspace_checks(ep):
+    c = small(ep)
+    n = ep.ep_workspace_size(c)
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_config_create(c, FAKE, n - 1)
+    assert ei.value.status == ep.EP_ERR_WORKSPACE
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_config_create(c, FAKE + 16, n)
+    assert ei.value.status == ep.EP_ERR_WORKSPACE
+    with pytest.raises(ep.EpError):
+        ep.ep_config_create(c, 0, n)
+    h = ep.ep_config_create(c, FAKE, n)
+    ep.ep_destroy(h)
+
+
+def test_state_machine_without_device(ep):
+    c = small(ep)
+    h = ep.ep_config_create(c, FAKE, ep.ep_workspace_size(c))
+    try:
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_combine(h, FAKE, FAKE, None, FAKE, None, 0, None)
+        assert ei.value.status == ep.EP_ERR_STATE
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_get_dispatch_src_token_pos(h)
+        assert ei.value.status == ep.EP_ERR_STATE
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_combine_standard_moe(h, FAKE, FAKE, None, FAKE, 0, None)
+        assert ei.value.status == ep.EP_ERR_STATE
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_convert_combine_input(h, FAKE, FAKE, None)
+        assert ei.value.status == ep.EP_ERR_STATE
+        # bad dispatch arguments are refused before any launch
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_dispatch(h, FAKE, FAKE, None, FAKE, [17] + [0] * 7, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_dispatch(h, FAKE + 8, FAKE, None, FAKE, [1] * 8, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_dispatch(h, None, FAKE, None, FAKE, [1] * 8, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        with pytest.raises(ep.EpError) as ei:        # standard_moe = 0
+            ep.ep_dispatch_standard_moe(h, FAKE, FAKE, None, FAKE, [1] * 8, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        ep.ep_reset(h)
+        assert "standard_moe" in ep.ep_last_error()
+    finally:
+        ep.ep_destroy(h)

@@ -1,0 +1,473 @@
+"""GPU parity: libep (through its C ABI) against the CPU oracle, bit for bit.
+
+Workload shapes follow the MORI-EP User Guide's DeepSeek-V3 example and
+benchmark tables; the small variants keep several 256-token chunks and a
+ragged tail so every tile path runs. Full-size cases compare all routing
+metadata exactly and payload / combine rows on a seeded sample.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_route_layout_gb300 import EpDispatchCombineOp, EpError
+from combine_route_layout_gb300 import ep as E
+from gen import WORKLOADS, make_expert_outputs
+from ep_harness import (DEV, Inputs, bits16, check_route, host, make_config, sample_rows,
+                        sample_tokens)
+
+pytestmark = pytest.mark.gpu
+
+
+def _out_bits(a: np.ndarray) -> np.ndarray:
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+def run_2d(wl, seed=None, ragged=False, full=True, nsample=192, cfg_over=None,
+           y_dtype=torch.bfloat16, want_weights=True):
+    cfg_over = dict(cfg_over or {})
+    inp = Inputs(wl, seed, ragged)
+    cfg = make_config(wl, combine_dtype=y_dtype, **cfg_over)
+    op = EpDispatchCombineOp(cfg)
+    R, T, H, Er = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.experts_per_rank
+    cap = R * T
+    d_x, d_w, d_sc, d_idx, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    torch.cuda.synchronize()
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    quant = cfg.quant_type != "none"
+
+    # weights and indices of every received row
+    w_ref = oracle.place_rows(inp.w, inp.ntok, slot)
+    idx_ref = oracle.place_rows(inp.idx, inp.ntok, slot)
+    gw, gi = host(d_w), host(d_idx)
+    for r in range(R):
+        n = recv[r]
+        assert np.array_equal(gw[r, :n].view(np.uint32), w_ref[r, :n].view(np.uint32)), r
+        assert np.array_equal(gi[r, :n], idx_ref[r, :n]), r
+
+    # payload (and FP8 scales)
+    if full:
+        xb = inp.x_bits()
+        if quant:
+            q, sc = oracle.quant_tokens(xb)
+            x_ref, sc_ref = oracle.place_rows(q, inp.ntok, slot), oracle.place_rows(sc, inp.ntok, slot)
+        else:
+            x_ref, sc_ref = oracle.place_rows(xb, inp.ntok, slot), None
+        gx = host(d_x)
+        gsc = host(d_sc) if quant else None
+        for r in range(R):
+            n = recv[r]
+            assert np.array_equal(gx[r, :n], x_ref[r, :n]), f"payload rank {r}"
+            if quant:
+                assert np.array_equal(gsc[r, :n].view(np.uint32), sc_ref[r, :n].view(np.uint32))
+    else:
+        rows = sample_rows(recv, nsample, seed=int(seed or 0))
+        rr = np.array([r for r, _ in rows])
+        ii = np.array([i for _, i in rows])
+        st = np.array([divmod(int(src_pos[r, i]), cap) for r, i in rows])
+        xb = inp.x_bits((st[:, 0], st[:, 1]))
+        gx = host(d_x[torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
+        if quant:
+            q, sc = oracle.quant_tokens(xb)
+            gsc = host(d_sc[torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
+            assert np.array_equal(gx, q), "sampled FP8 codes"
+            assert np.array_equal(gsc.view(np.uint32), sc.view(np.uint32)), "sampled scales"
+        else:
+            assert np.array_equal(gx, xb), "sampled payload"
+
+    # combine
+    if wl.expert_output == "identity":
+        assert not quant
+        y_d = d_x
+        y_ref = x_ref if full else None
+    else:
+        y_d = make_expert_outputs(wl, cap, seed, device=DEV, dtype=y_dtype)
+        y_ref = host(y_d)
+    od = "fp32" if cfg.combine_out_dtype == torch.float32 else "bf16"
+    out_d, outw_d = op.combine(y_d, d_w, inp.idx_d, call_reset=True, want_weights=want_weights)
+    op.sync()
+    go = host(out_d)
+    if y_ref is None:
+        y_ref = host(y_d)
+    if full:
+        out_ref, outw_ref = oracle.combine(y_ref, inp.idx, inp.ntok, slot, Er, w_recv=w_ref,
+                                           weighted=cfg.weighted_combine, out_dtype=od)
+        gow = host(outw_d) if outw_d is not None else None
+        for s in range(R):
+            n = inp.ntok[s]
+            assert np.array_equal(_out_bits(go[s, :n]), _out_bits(out_ref[s, :n])), f"combine rank {s}"
+            if gow is not None:
+                assert np.array_equal(gow[s, :n].view(np.uint32), outw_ref[s, :n].view(np.uint32))
+    else:
+        toks = sample_tokens(wl, inp.ntok, 4 * nsample, seed=int(seed or 0))
+        out_ref, outw_ref = oracle.combine_tokens(toks, y_ref, inp.idx, slot, Er, w_recv=w_ref,
+                                                  weighted=cfg.weighted_combine, out_dtype=od)
+        s_, t_ = toks // T, toks % T
+        got = go[s_, t_]
+        assert np.array_equal(_out_bits(got), _out_bits(out_ref)), "sampled combine"
+        if outw_d is not None:
+            gow = host(outw_d)[s_, t_]
+            assert np.array_equal(gow.view(np.uint32), outw_ref.view(np.uint32))
+    return op
+
+
+# ------------------------------------------------------------- small shapes
+
+@pytest.mark.parametrize("seed,ragged", [(0, False), (1, True), (2, False)])
+def test_tiny_identity(seed, ragged):
+    run_2d(WORKLOADS["tiny"], seed=seed, ragged=ragged)
+
+
+def test_ds_v3_latency_full():
+    run_2d(WORKLOADS["ds_v3_latency"])
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_ds_v3_latency_seeds(seed):
+    run_2d(WORKLOADS["ds_v3_latency"], seed=seed, ragged=True)
+
+
+def test_throughput_shape_small_ragged():
+    wl = WORKLOADS["ds_v3_throughput"].with_(tokens_per_rank=300)
+    run_2d(wl, seed=3, ragged=True)
+
+
+def test_mid_shape_small_ragged():
+    wl = WORKLOADS["mid_masked"].with_(tokens_per_rank=600)
+    run_2d(wl, seed=4, ragged=True)
+
+
+@pytest.mark.parametrize("over", [
+    dict(world_size=1, experts_per_rank=8, topk=4),
+    dict(world_size=32, experts_per_rank=2, topk=8, tokens_per_rank=40),
+    dict(world_size=4, experts_per_rank=3, topk=1),
+    dict(world_size=8, experts_per_rank=4, topk=16),
+    dict(hidden=384),
+    dict(hidden=264),
+    dict(mask_prob=1.0),
+    dict(mask_prob=0.6, tokens_per_rank=257),
+])
+def test_edge_shapes(over):
+    wl = WORKLOADS["tiny"].with_(**over)
+    run_2d(wl, seed=5, ragged=True)
+
+
+def test_empty_ranks():
+    wl = WORKLOADS["tiny"]
+    inp_ntok = np.zeros(wl.world_size, np.int32)
+    inp = Inputs(wl, 0)
+    op = EpDispatchCombineOp(make_config(wl))
+    d_x, d_w, _, _, recv = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp_ntok)
+    out, _ = op.combine(d_x, d_w, None, call_reset=True)
+    op.sync()
+    assert int(recv.sum()) == 0
+
+
+@pytest.mark.parametrize("yd,od", [(torch.float32, torch.float32), (torch.float32, torch.bfloat16),
+                                   (torch.bfloat16, torch.bfloat16)])
+def test_combine_dtypes(yd, od):
+    wl = WORKLOADS["mid_masked"].with_(tokens_per_rank=100, hidden=512, expert_output="random")
+    run_2d(wl, seed=6, ragged=True, y_dtype=yd, cfg_over=dict(combine_out_dtype=od))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_weighted_2d_combine(fp8):
+    wl = WORKLOADS["mid_masked"].with_(tokens_per_rank=130, hidden=1024, weighted=True,
+                                       dispatch_dtype="fp8" if fp8 else "bf16")
+    run_2d(wl, seed=7, ragged=True)
+
+
+def test_fp8_passthrough_with_scales():
+    """Dispatch carries already-quantised FP8 payloads and their scales
+    ("Choosing an EP API and backend", EP paths table)."""
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=70, hidden=1024)
+    R, T, H, k = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.topk
+    inp = Inputs(wl, 8, ragged=True)
+    codes = torch.randint(0, 256, (R, T, H), dtype=torch.uint8, device=DEV)
+    codes[codes == 0x7F] = 0
+    codes[codes == 0xFF] = 0
+    xq = codes.view(torch.float8_e4m3fn)
+    scales = torch.rand((R, T, H // 128), device=DEV, dtype=torch.float32)
+    cfg = make_config(wl, data_type=torch.float8_e4m3fn, quant_type="none", scale_dim=H // 128,
+                      scale_type_size=4)
+    op = EpDispatchCombineOp(cfg)
+    d_x, d_w, d_sc, d_idx, recv_d = op.dispatch(xq, inp.w_d, scales, inp.idx_d, inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    x_ref = oracle.place_rows(host(codes), inp.ntok, slot)
+    sc_ref = oracle.place_rows(host(scales), inp.ntok, slot)
+    gx, gs = host(d_x), host(d_sc).view(np.float32)
+    for r in range(R):
+        n = recv[r]
+        assert np.array_equal(gx[r, :n], x_ref[r, :n])
+        assert np.array_equal(gs[r, :n].reshape(n, -1).view(np.uint32),
+                              sc_ref[r, :n].view(np.uint32))
+    op.reset()
+
+
+# --------------------------------------------------------------- full sizes
+
+@pytest.mark.slow
+def test_ds_v3_throughput_full_size():
+    run_2d(WORKLOADS["ds_v3_throughput"], full=False)
+
+
+@pytest.mark.slow
+def test_mid_masked_full_size():
+    run_2d(WORKLOADS["mid_masked"], full=False)
+
+
+@pytest.mark.slow
+def test_tiny_full_size_seed0():
+    run_2d(WORKLOADS["tiny"])
+
+
+# ------------------------------------------------------------ standard MoE
+
+def _pcap(wl):
+    return wl.world_size * wl.tokens_per_rank * min(wl.topk, wl.experts_per_rank) + \
+        127 * wl.experts_per_rank
+
+
+def run_std(wl, seed=None, ragged=False, full=True, nsample=256, cfg_over=None):
+    cfg_over = dict(cfg_over or {})
+    inp = Inputs(wl, seed, ragged)
+    cfg = make_config(wl, standard_moe=True, **cfg_over)
+    op = EpDispatchCombineOp(cfg)
+    R, T, H, Er = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.experts_per_rank
+    v = op.dispatch_standard_moe(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    op.sync()
+    pcap = op.pcap
+    assert pcap == _pcap(wl) or cfg.max_packed_rows_per_rank > 0
+    ref = oracle.std_layout(inp.idx, inp.ntok, Er, pcap)
+    assert np.array_equal(host(v["packed_recv_count"]), ref["count"])
+    assert np.array_equal(host(v["expert_offset"]), ref["seg_off"])
+    assert np.array_equal(host(v["rank_rows"]), ref["rank_rows"])
+    assert np.array_equal(host(v["packed_recv_layout_range"]), ref["layout_range"])
+    gsi = host(v["packed_recv_src_info"])
+    for r in range(R):
+        n = ref["rank_rows"][r]
+        assert np.array_equal(gsi[r, :n], ref["src_info"][r, :n]), f"src_info rank {r}"
+    quant = cfg.quant_type != "none"
+    data = [(r, i) for r in range(R) for i in np.nonzero(ref["src_info"][r] >= 0)[0]]
+    if not full:
+        rng = np.random.default_rng(1)
+        data = [data[j] for j in np.sort(rng.choice(len(data), size=min(len(data), 8 * nsample),
+                                                    replace=False))]
+    rr = np.array([r for r, _ in data])
+    ii = np.array([i for _, i in data])
+    st = np.array([divmod(int(ref["src_info"][r, i]), R * T) for r, i in data])
+    xb = inp.x_bits((st[:, 0], st[:, 1]))
+    gx = host(v["packed_recv_x"][torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
+    if quant:
+        q, sc = oracle.quant_tokens(xb)
+        gsc = host(v["packed_recv_scales"][torch.as_tensor(rr, device=DEV),
+                                           torch.as_tensor(ii, device=DEV)])
+        assert np.array_equal(gx, q)
+        assert np.array_equal(gsc.view(np.uint32), sc.view(np.uint32))
+    else:
+        assert np.array_equal(gx, xb), "packed payload"
+
+    # combine_standard_moe on random packed expert outputs
+    Y = make_expert_outputs(wl, pcap, seed, device=DEV, dtype=cfg.combine_dtype)
+    out_d = op.combine_standard_moe(Y, inp.w_d, inp.idx_d, call_reset=True)
+    op.sync()
+    od = "fp32" if cfg.combine_out_dtype == torch.float32 else "bf16"
+    toks = (np.array([s * T + t for s in range(R) for t in range(int(inp.ntok[s]))], np.int64)
+            if full else sample_tokens(wl, inp.ntok, 4 * nsample))
+    # gather the rows the sampled tokens use (oracle layout) into a compact Y
+    rm = ref["row_map"].reshape(-1, wl.topk)[toks]
+    used = np.unique(rm[rm >= 0])
+    remap = np.full(R * pcap, -1, np.int64)
+    remap[used] = np.arange(len(used))
+    Ysub = host(Y.view(R * pcap, H)[torch.as_tensor(used, device=DEV)])
+    rm_sub = np.full((R * T, wl.topk), -1, np.int32)
+    rm_sub[toks] = np.where(rm >= 0, remap[np.maximum(rm, 0)], -1)
+    out_ref = oracle.std_combine_tokens(toks, Ysub, inp.idx, rm_sub.reshape(R, T, wl.topk), Er,
+                                        w=inp.w, weighted=cfg.weighted_combine, out_dtype=od)
+    got = host(out_d)[toks // T, toks % T]
+    assert np.array_equal(_out_bits(got), _out_bits(out_ref)), "combine_standard_moe"
+    return op
+
+
+def test_skewed_std_small():
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=300)
+    run_std(wl, seed=1, ragged=True)
+
+
+@pytest.mark.parametrize("over", [dict(router="uniform", mask_prob=0.2),
+                                  dict(dispatch_dtype="fp8", tokens_per_rank=90),
+                                  dict(weighted=False, combine_out_dtype="bf16"),
+                                  dict(world_size=4, experts_per_rank=5, topk=3, hidden=384)])
+def test_std_variants(over):
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=200, hidden=1024).with_(**over)
+    run_std(wl, seed=2, ragged=True)
+
+
+@pytest.mark.slow
+def test_skewed_std_full_size():
+    run_std(WORKLOADS["skewed_zipf_std_moe"], full=False)
+
+
+# ------------------------------------------------------------- conversions
+
+def test_convert_round_trip():
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=260, hidden=1024, mask_prob=0.1)
+    R, T, H, Er, k = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.experts_per_rank, wl.topk
+    inp = Inputs(wl, 3, ragged=True)
+    cfg = make_config(wl, standard_moe=True, combine_dtype=torch.bfloat16,
+                      combine_out_dtype=torch.float32, weighted_combine=False)
+    op = EpDispatchCombineOp(cfg)
+    d_x, d_w, _, d_idx, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    px, pcount, psrc, prange = op.convert_dispatch_output(d_x, d_idx)
+    op.sync()
+    pcap = op.pcap
+    ref = oracle.std_dispatch(inp.x_bits(), inp.idx, inp.ntok, Er, pcap)
+    assert np.array_equal(host(pcount), ref["count"])
+    assert np.array_equal(host(prange), ref["layout_range"])
+    gsi = host(psrc)
+    gx = host(px)
+    for r in range(R):
+        n = ref["rank_rows"][r]
+        assert np.array_equal(gsi[r, :n], ref["src_info"][r, :n])
+        used = ref["src_info"][r, :n] >= 0
+        assert np.array_equal(gx[r, :n][used], ref["x"][r, :n][used])
+
+    recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, Er)
+    Y = make_expert_outputs(wl, pcap, 3, device=DEV)
+    y2d = op.convert_combine_input(px, psrc, prange)
+    Yh = host(Y)
+    y2d_ref = oracle.convert_combine_input(Yh, recv, src_pos, inp.idx, ref["row_map"], Er,
+                                           out_dtype="bf16")
+    gy = host(y2d)
+    for r in range(R):
+        assert np.array_equal(gy[r, :recv[r]], y2d_ref[r, :recv[r]]), f"convert_combine_input {r}"
+    out_d, _ = op.combine(y2d, d_w, None)
+    out_ref, _ = oracle.combine(y2d_ref, inp.idx, inp.ntok, slot, Er, out_dtype="fp32")
+    go = host(out_d)
+    for s in range(R):
+        n = inp.ntok[s]
+        assert np.array_equal(go[s, :n].view(np.uint32), out_ref[s, :n].view(np.uint32))
+    # the packed layout from the conversion also feeds combine_standard_moe
+    out_std = op.combine_standard_moe(Y, None, None, call_reset=True)
+    ref_std = oracle.std_combine(Yh, inp.idx, inp.ntok, ref["row_map"], Er, weighted=False,
+                                 out_dtype="fp32")
+    gs = host(out_std)
+    for s in range(R):
+        n = inp.ntok[s]
+        assert np.array_equal(gs[s, :n].view(np.uint32), ref_std[s, :n].view(np.uint32))
+
+
+# ------------------------------------------------------------ error flags
+
+def test_invalid_index_sets_error_flag():
+    wl = WORKLOADS["tiny"]
+    inp = Inputs(wl, 0)
+    idx = inp.idx.copy()
+    idx[2, 3, 1] = wl.num_experts          # out of range
+    op = EpDispatchCombineOp(make_config(wl))
+    op.dispatch(inp.x, inp.w_d, None, torch.from_numpy(idx).to(DEV), inp.ntok)
+    with pytest.raises(EpError) as ei:
+        op.sync()
+    assert ei.value.status == E.EP_ERR_INVALID_INDEX
+    op.sync()                               # flag cleared
+    op.reset()
+
+
+def test_std_capacity_overflow_flagged():
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=100, hidden=256)
+    inp = Inputs(wl, 0)
+    op = EpDispatchCombineOp(make_config(wl, standard_moe=True, max_packed_rows_per_rank=256))
+    op.dispatch_standard_moe(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    with pytest.raises(EpError) as ei:
+        op.sync()
+    assert ei.value.status == E.EP_ERR_CAPACITY
+    op.reset()
+
+
+def test_std_duplicate_ids_flagged():
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=20, hidden=256)
+    inp = Inputs(wl, 0)
+    idx = inp.idx.copy()
+    idx[1, 2, 3] = idx[1, 2, 0]
+    op = EpDispatchCombineOp(make_config(wl, standard_moe=True))
+    op.dispatch_standard_moe(inp.x, inp.w_d, None, torch.from_numpy(idx).to(DEV), inp.ntok)
+    with pytest.raises(EpError) as ei:
+        op.sync()
+    assert ei.value.status == E.EP_ERR_INVALID_INDEX
+    op.reset()
+
+
+# ------------------------------------------- invariants and repeated rounds
+
+def test_identity_invariant_bf16_dispatch():
+    """Identity experts: combine returns the token times its number of
+    distinct destination ranks (exact in f32 since |D| <= 8)."""
+    wl = WORKLOADS["mid_masked"].with_(tokens_per_rank=512, combine_out_dtype="fp32")
+    inp = Inputs(wl, 9, ragged=True)
+    op = EpDispatchCombineOp(make_config(wl))
+    d_x, d_w, _, _, _ = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    out, _ = op.combine(d_x, d_w, None, call_reset=True)
+    owners = torch.where(inp.idx_d >= 0, inp.idx_d // wl.experts_per_rank, -1)
+    nD = torch.zeros(owners.shape[:2], dtype=torch.float32, device=DEV)
+    for r in range(wl.world_size):
+        nD += (owners == r).any(-1).float()
+    exp = inp.x.float() * nD[..., None]
+    for s in range(wl.world_size):
+        n = int(inp.ntok[s])
+        assert torch.equal(out[s, :n], exp[s, :n])
+
+
+def test_repeated_rounds_random_shapes():
+    """Many dispatch -> combine -> reset rounds with changing token counts on
+    one handle (the tuning guide's repeated-round verification)."""
+    wl = WORKLOADS["tiny"].with_(tokens_per_rank=64, hidden=256)
+    inp = Inputs(wl, 0)
+    op = EpDispatchCombineOp(make_config(wl))
+    rng = np.random.default_rng(0)
+    R, T = wl.world_size, wl.tokens_per_rank
+    owners = torch.where(inp.idx_d >= 0, inp.idx_d // wl.experts_per_rank, -1)
+    nD = torch.zeros(owners.shape[:2], dtype=torch.float32, device=DEV)
+    for r in range(R):
+        nD += (owners == r).any(-1).float()
+    exp = inp.x.float() * nD[..., None]
+    for it in range(200):
+        ntok = rng.integers(0, T + 1, size=R).astype(np.int32)
+        d_x, d_w, _, _, recv = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, ntok)
+        out, _ = op.combine(d_x, d_w, None, call_reset=True)
+        if it % 25 == 0:
+            op.sync()
+            for s in range(R):
+                assert torch.equal(out[s, :ntok[s]], exp[s, :ntok[s]].to(out.dtype))
+    op.sync()
+
+
+def test_cuda_graph_capture_replay():
+    """Dispatch + combine make no host synchronisation, so they capture into a
+    CUDA graph and replay with the same results."""
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=64)
+    inp = Inputs(wl, 0)
+    op = EpDispatchCombineOp(make_config(wl))
+    cap = wl.world_size * wl.tokens_per_rank
+    y = make_expert_outputs(wl, cap, 0, device=DEV)
+    out = torch.empty((wl.world_size, wl.tokens_per_rank, wl.hidden), dtype=torch.bfloat16,
+                      device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, None)   # warm-up (first-call set-up)
+        op.combine(y, d[1], None, out=out, call_reset=True)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, None)
+        op.combine(y, d[1], None, out=out, call_reset=True)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
