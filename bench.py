@@ -1,0 +1,522 @@
+"""Benchmark: MoE expert-parallel dispatch + combine on simulated EP ranks.
+
+One step = ep_dispatch (routing layout + payload kernel) followed by
+ep_combine with call_reset (combine kernel), on inputs resident in HBM.
+Default workload: DeepSeek-V3 prefill shape from the MORI-EP User Guide's
+benchmark table (8 ranks x 32 experts, 4096 tokens/rank, hidden 7168, top-8,
+FP8 E4M3 dispatch with per-128 scales, bf16 combine); its inputs are larger
+than L2. The 128-token decode shape is also timed (with an L2 flush between
+iterations) and reported under "latency_shape".
+
+Prints one JSON line. `--impl reference` times the CPU oracle (plain
+single-threaded C) on a bounded sample of the same workload instead.
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload on its own GPU (the simulated EP group fits one GPU); value is the
+sum over ranks, time the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gen import WORKLOADS, make_expert_outputs, make_indices, make_num_tokens, make_tokens, \
+    make_weights  # noqa: E402
+
+METRIC = "dispatch/combine µs and effective GB/s at 128 & 4096 tok/rank; % of HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------ byte model
+
+def algorithmic_bytes(wl, C: int, P: int, Ttot: int) -> dict:
+    """Bytes each step must move (reads + writes), counted from the routing.
+
+    2D dispatch reads every token once (payload + weights + ids) and writes
+    one received row per (token, destination rank): payload, FP8 scales,
+    weights, ids and its src_token_pos. 2D combine reads one expert-output row
+    plus its weights and slot per copy and writes the token's output row and
+    weights. Standard MoE moves one row per valid (token, slot).
+    """
+    H, k = wl.hidden, wl.topk
+    nb = H // 128
+    fp8 = wl.dispatch_dtype == "fp8"
+    b = 1 if fp8 else 2
+    bo = 4 if wl.combine_out_dtype == "fp32" else 2
+    if not wl.standard_moe:
+        d_read = Ttot * (2 * H + 8 * k)
+        d_write = C * (H * b + (4 * nb if fp8 else 0) + 8 * k + 4)
+        c_read = C * (2 * H + 4 * k + 4)
+        c_write = Ttot * (H * bo + 4 * k)
+    else:
+        d_read = Ttot * (2 * H + 8 * k)
+        d_write = P * (H * b + (4 * nb if fp8 else 0) + 4)
+        c_read = P * (2 * H + 4) + Ttot * 8 * k
+        c_write = Ttot * bo * H
+    return {"dispatch": d_read + d_write, "combine": c_read + c_write,
+            "dispatch_read": d_read, "dispatch_write": d_write,
+            "combine_read": c_read, "combine_write": c_write}
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_key: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel
+    source has not changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[kernel_key]
+        src = os.path.join(ROOT, rec["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != rec["source_sha256_16"]:
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.result = None
+        if not self.proc:
+            return
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                           "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- our arm
+
+def make_op(wl, device):
+    from combine_route_layout_gb300 import EpDispatchCombineConfig, EpDispatchCombineOp
+    cfg = EpDispatchCombineConfig(
+        data_type=torch.bfloat16, world_size=wl.world_size, hidden_dim=wl.hidden, scale_dim=0,
+        scale_type_size=4, max_token_type_size=4,
+        max_num_inp_token_per_rank=wl.tokens_per_rank,
+        num_experts_per_rank=wl.experts_per_rank, num_experts_per_token=wl.topk,
+        quant_type="fp8_e4m3_block128" if wl.dispatch_dtype == "fp8" else "none",
+        combine_dtype=torch.bfloat16,
+        combine_out_dtype=torch.float32 if wl.combine_out_dtype == "fp32" else torch.bfloat16,
+        weighted_combine=wl.weighted, standard_moe=wl.standard_moe)
+    return EpDispatchCombineOp(cfg, device)
+
+
+class Step:
+    """Device-resident inputs and one dispatch + combine step."""
+
+    def __init__(self, wl, device, seed=0):
+        self.wl = wl
+        self.dev = device
+        self.op = make_op(wl, device)
+        self.x = make_tokens(wl, seed, device=device)
+        self.idx = torch.from_numpy(make_indices(wl, seed)).to(device)
+        self.w = torch.from_numpy(make_weights(wl, seed)).to(device)
+        self.ntok = make_num_tokens(wl)
+        R, T = wl.world_size, wl.tokens_per_rank
+        if wl.standard_moe:
+            v = self.op.dispatch_standard_moe(self.x, self.w, None, self.idx, self.ntok)
+            torch.cuda.synchronize()
+            self.counts = v["packed_recv_count"].sum().item()
+            self.rank_rows = v["rank_rows"].cpu().numpy()
+            rows = self.op.pcap
+        else:
+            d = self.op.dispatch(self.x, self.w, None, self.idx, self.ntok)
+            torch.cuda.synchronize()
+            self.recv = d[4].cpu().numpy()
+            rows = R * T
+        self.op.reset()
+        self.op.sync()
+        self.y = make_expert_outputs(wl, rows, seed, device=device)
+        self.out = torch.empty((R, T, wl.hidden),
+                               dtype=torch.float32 if wl.combine_out_dtype == "fp32"
+                               else torch.bfloat16, device=device)
+        self.out_w = torch.empty((R, T, wl.topk), dtype=torch.float32, device=device)
+        Ttot = int(self.ntok.sum())
+        C = 0 if wl.standard_moe else int(self.recv.sum())
+        P = int(self.counts) if wl.standard_moe else 0
+        self.bytes = algorithmic_bytes(wl, C, P, Ttot)
+        self.C, self.P, self.Ttot = C, P, Ttot
+
+    def dispatch(self, x=None, w=None, idx=None):
+        x = self.x if x is None else x
+        w = self.w if w is None else w
+        idx = self.idx if idx is None else idx
+        if self.wl.standard_moe:
+            return self.op.dispatch_standard_moe(x, w, None, idx, self.ntok)
+        return self.op.dispatch(x, w, None, idx, self.ntok)
+
+    def combine(self, d, y=None, w=None):
+        y = self.y if y is None else y
+        if self.wl.standard_moe:
+            self.op.combine_standard_moe(y, self.w if w is None else w, None, out=self.out,
+                                         call_reset=True)
+        else:
+            self.op.combine(y, d[1], None, out=self.out, out_weights=self.out_w, call_reset=True)
+
+
+def time_steps(step: Step, K: int, W: int, flush: torch.Tensor | None, dist_barrier):
+    st = torch.cuda.current_stream()
+    for _ in range(W):
+        d = step.dispatch()
+        step.combine(d)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    dist_barrier()
+    torch.cuda.synchronize()
+    t0.record(st)
+    for i in range(K):
+        if flush is not None:
+            flush.add_(1)              # evict L2 between iterations (outside the kernel events)
+        ev[i][0].record(st)
+        d = step.dispatch()
+        ev[i][1].record(st)
+        step.combine(d)
+        ev[i][2].record(st)
+    t1.record(st)
+    torch.cuda.synchronize()
+    dist_barrier()
+    total_ms = t0.elapsed_time(t1)
+    disp = [e[0].elapsed_time(e[1]) for e in ev]
+    comb = [e[1].elapsed_time(e[2]) for e in ev]
+    return total_ms, disp, comb
+
+
+def time_e2e(step: Step, K: int, W: int, dist_barrier):
+    """Same step through the public API with pinned host inputs: H2D of the
+    step's inputs (tokens, weights, ids, the expert-output rows that will be
+    read) and D2H of the combined output, all inside the timed region."""
+    wl = step.wl
+    st = torch.cuda.current_stream()
+    xh = step.x.cpu().pin_memory()
+    wh = step.w.cpu().pin_memory()
+    ih = step.idx.cpu().pin_memory()
+    # only the expert-output rows the combine reads travel
+    used = step.rank_rows if wl.standard_moe else step.recv
+    ycopy, ybytes = [], 0
+    for r in range(wl.world_size):
+        n = int(used[r])
+        if n == 0:
+            continue
+        h = step.y[r, :n].cpu().pin_memory()
+        ycopy.append((h, step.y[r, :n]))
+        ybytes += h.numel() * h.element_size()
+    oh = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    xd = torch.empty_like(step.x)
+    wd = torch.empty_like(step.w)
+    idd = torch.empty_like(step.idx)
+    h2d = xh.numel() * xh.element_size() + wh.numel() * 4 + ih.numel() * 4 + ybytes
+    d2h = oh.numel() * oh.element_size()
+
+    def one():
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        idd.copy_(ih, non_blocking=True)
+        for hsrc, ddst in ycopy:
+            ddst.copy_(hsrc, non_blocking=True)
+        d = step.dispatch(xd, wd, idd)
+        step.combine(d, w=wd)
+        oh.copy_(step.out, non_blocking=True)
+
+    for _ in range(max(1, W)):
+        one()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    dist_barrier()
+    t0.record(st)
+    for _ in range(K):
+        one()
+    t1.record(st)
+    torch.cuda.synchronize()
+    dist_barrier()
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def cpu_oracle_step(wl, tokens_per_rank: int, seed: int = 0, y=None):
+    """One dispatch + combine of the workload restricted to `tokens_per_rank`
+    tokens per source rank, on the CPU oracle. Returns (seconds, bytes)."""
+    import oracle
+    sw = wl.with_(tokens_per_rank=tokens_per_rank)
+    idx = make_indices(sw, seed)
+    w = make_weights(sw, seed)
+    x = make_tokens(sw, seed).view(torch.int16).numpy().view(np.uint16)
+    ntok = make_num_tokens(sw)
+    R, T = sw.world_size, sw.tokens_per_rank
+    Er = sw.experts_per_rank
+    od = "fp32" if sw.combine_out_dtype == "fp32" else "bf16"
+    if sw.standard_moe:
+        pcap = R * T * min(sw.topk, Er) + 127 * Er
+        if y is None:
+            y = make_expert_outputs(sw, pcap, seed).view(torch.int16).numpy().view(np.uint16)
+        t = time.perf_counter()
+        res = oracle.std_dispatch(x, idx, ntok, Er, pcap, quant_fp8=sw.dispatch_dtype == "fp8")
+        oracle.std_combine(y, idx, ntok, res["row_map"], Er, w=w, weighted=sw.weighted,
+                           out_dtype=od)
+        dt = time.perf_counter() - t
+        P = int(res["count"].sum())
+        b = algorithmic_bytes(sw, 0, P, int(ntok.sum()))
+    else:
+        if y is None:
+            y = make_expert_outputs(sw, R * T, seed).view(torch.int16).numpy().view(np.uint16)
+        t = time.perf_counter()
+        d = oracle.dispatch(x, w, idx, ntok, Er, quant_fp8=sw.dispatch_dtype == "fp8")
+        oracle.combine(y, idx, ntok, d["slot"], Er, w_recv=d["w"], weighted=sw.weighted,
+                       out_dtype=od)
+        dt = time.perf_counter() - t
+        b = algorithmic_bytes(sw, int(d["recv_num_token"].sum()), 0, int(ntok.sum()))
+    return dt, b["dispatch"] + b["combine"], y
+
+
+def cpu_baseline(wl, sample_tokens: int, reps: int):
+    dt_tot, by_tot, y = 0.0, 0, None
+    for _ in range(reps):
+        dt, by, y = cpu_oracle_step(wl, sample_tokens, y=y)
+        dt_tot += dt
+        by_tot += by
+    gbs = by_tot / dt_tot / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{wl.name} restricted to {sample_tokens} tokens/rank "
+                      f"({wl.world_size * sample_tokens} tokens), {reps} dispatch+combine "
+                      f"passes, single-threaded C, {dt_tot:.1f} s"}
+
+
+# ----------------------------------------------------------- main
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier_fn(world):
+    if world <= 1:
+        return lambda: None
+    import torch.distributed as dist
+
+    def b():
+        dist.barrier()
+    return b
+
+
+def reduce_max(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return None
+    steps, warm = args.steps, args.warmup
+    T = args.ref_tokens
+    y = None
+    for _ in range(warm):
+        _, _, y = cpu_oracle_step(wl, T, y=y)
+    tot, by = 0.0, 0
+    for _ in range(steps):
+        dt, b, y = cpu_oracle_step(wl, T, y=y)
+        tot += dt
+        by += b
+    gbs = by / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": round(tot / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "sample_tokens_per_rank": T, "world_size": wl.world_size,
+                   "experts_per_rank": wl.experts_per_rank, "hidden": wl.hidden, "topk": wl.topk},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{T} tokens/rank per step, single-threaded C oracle"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="ds_v3_throughput", choices=sorted(WORKLOADS))
+    ap.add_argument("--latency-workload", default="ds_v3_latency")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-latency", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=512,
+                    help="tokens/rank of the CPU-oracle baseline sample")
+    ap.add_argument("--cpu-reps", type=int, default=2)
+    ap.add_argument("--ref-tokens", type=int, default=128,
+                    help="tokens/rank per step of the reference (oracle) arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local = dist_setup(args.gpus)
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    barrier = barrier_fn(world)
+    step = Step(wl, dev)
+    peak, peak_src = hbm_peak()
+    with ClockSampler(local) as clk:
+        total_ms, disp, comb = time_steps(step, args.steps, args.warmup, None, barrier)
+    total_ms = reduce_max(total_ms, world)
+    K = args.steps
+    per_step = total_ms / K
+    b = step.bytes
+    step_bytes = b["dispatch"] + b["combine"]
+    value = step_bytes * world / (per_step * 1e-3) / 1e9
+    d_us = statistics.median(disp) * 1e3
+    c_us = statistics.median(comb) * 1e3
+    d_mean = statistics.mean(disp) * 1e3
+    c_mean = statistics.mean(comb) * 1e3
+    d_gbs = b["dispatch"] / (d_mean * 1e-6) / 1e9
+    c_gbs = b["combine"] / (c_mean * 1e-6) / 1e9
+    dom = "combine" if c_mean >= d_mean else "dispatch"
+    dom_key = {"combine": "combine_2d" if not wl.standard_moe else "combine_std",
+               "dispatch": "dispatch_2d" if not wl.standard_moe else "dispatch_std"}[dom]
+    ach = c_gbs if dom == "combine" else d_gbs
+    tr = profiled_traffic(dom_key)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "world_size": wl.world_size,
+                   "experts_per_rank": wl.experts_per_rank, "tokens_per_rank": wl.tokens_per_rank,
+                   "hidden": wl.hidden, "topk": wl.topk, "dispatch_payload": wl.dispatch_dtype,
+                   "combine_out": wl.combine_out_dtype, "standard_moe": wl.standard_moe,
+                   "l2": "inputs larger than L2 (129 MB); no flush",
+                   "copies_C": step.C, "packed_rows_P": step.P,
+                   "parallelism": f"replicas x{world}, 8 simulated EP ranks each"},
+        "dispatch": {"us_median": round(d_us, 2), "us_mean": round(d_mean, 2),
+                     "bytes": b["dispatch"], "GBps": round(d_gbs, 1),
+                     "frac_of_peak": round(d_gbs / peak, 4)},
+        "combine": {"us_median": round(c_us, 2), "us_mean": round(c_mean, 2),
+                    "bytes": b["combine"], "GBps": round(c_gbs, 1),
+                    "frac_of_peak": round(c_gbs / peak, 4)},
+        "roofline": {"bound": "hbm", "kernel": dom_key, "achieved": round(ach, 1),
+                     "peak": peak, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(ach / peak, 4),
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None},
+        "clocks": clk.result,
+        "gpu_launches": 3 * K,
+    }
+
+    if not args.no_latency and rank == 0:
+        lw = WORKLOADS[args.latency_workload]
+        ls = Step(lw, dev)
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        lk = max(50, K)
+        _, ld, lc = time_steps(ls, lk, max(args.warmup, 5), flush, lambda: None)
+        lb = ls.bytes
+        line["latency_shape"] = {
+            "workload": lw.name, "iters": lk, "l2": "flushed (256 MB write) before each step",
+            "dispatch_us_median": round(statistics.median(ld) * 1e3, 2),
+            "combine_us_median": round(statistics.median(lc) * 1e3, 2),
+            "dispatch_GBps": round(lb["dispatch"] / (statistics.median(ld) * 1e-3) / 1e9, 1),
+            "combine_GBps": round(lb["combine"] / (statistics.median(lc) * 1e-3) / 1e9, 1),
+        }
+        del ls, flush
+
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(step, K, args.warmup, barrier)
+        e_ms = reduce_max(e_ms, world)
+        line["e2e"] = {"value": round(step_bytes * world / (e_ms / K * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                       "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / K, 3)}
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_tokens, args.cpu_reps)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

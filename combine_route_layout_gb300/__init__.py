@@ -1,7 +1,17 @@
 """GB300-native MoE expert-parallel dispatch / combine (simulated EP ranks on one GPU).
 
 The compute lives in libep.so (hand-written sm_103a CUDA kernels behind the C
-ABI of include/ep.h); `ep` is its thin Python binding.
+ABI of include/ep.h); `ep` is its thin Python binding. The binding is loaded
+on first use, so `combine_route_layout_gb300.build` can run before the
+library exists; any other use fails loudly if the library is missing.
 """
-from . import ep  # noqa: F401
-from .ep import EpDispatchCombineConfig, EpDispatchCombineOp, EpError  # noqa: F401
+
+_EXPORTS = ("EpDispatchCombineConfig", "EpDispatchCombineOp", "EpError")
+
+
+def __getattr__(name):
+    if name == "ep" or name in _EXPORTS:
+        import importlib
+        ep = importlib.import_module(".ep", __name__)
+        return ep if name == "ep" else getattr(ep, name)
+    raise AttributeError(name)
