@@ -416,6 +416,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ds_v3_throughput", choices=sorted(WORKLOADS))
     ap.add_argument("--latency-workload", default="ds_v3_latency")
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="override the workload's tokens per rank (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
@@ -430,6 +432,8 @@ def main():
 
     rank, world, local = dist_setup(args.gpus)
     wl = WORKLOADS[args.workload]
+    if args.tokens_per_rank > 0:
+        wl = wl.with_(tokens_per_rank=args.tokens_per_rank)
     if args.impl == "reference":
         line = run_reference(args, wl, rank, world)
         if line is not None:

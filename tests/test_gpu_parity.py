@@ -336,7 +336,7 @@ def test_convert_round_trip():
 
     recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, Er)
     Y = make_expert_outputs(wl, pcap, 3, device=DEV)
-    y2d = op.convert_combine_input(px, psrc, prange)
+    y2d = op.convert_combine_input(Y, psrc, prange)
     Yh = host(Y)
     y2d_ref = oracle.convert_combine_input(Yh, recv, src_pos, inp.idx, ref["row_map"], Er,
                                            out_dtype="bf16")
