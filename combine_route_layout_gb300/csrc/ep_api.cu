@@ -214,6 +214,11 @@ ep_status device_sm_count(int* out) {
 
 }  // namespace
 
+ep_status ep::record_error(ep_status st, const char* msg) {
+  g_last_error = msg;
+  return st;
+}
+
 struct ep_handle {
   ep_config cfg;
   Geometry g;

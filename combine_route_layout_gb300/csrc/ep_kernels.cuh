@@ -169,6 +169,9 @@ cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
 cudaError_t launch_convert_combine(const ConvertParams& p, int dtype, const LaunchCfg& lc,
                                    cudaStream_t st);
 
+// Record `msg` as the calling thread's ep_last_error() text; returns `st`.
+ep_status record_error(ep_status st, const char* msg);
+
 // Work-unit geometry used by the launchers and the host library alike.
 constexpr int kCopyUnroll = 4;       // 16-byte vectors per lane per copy unit
 constexpr int kQuantUnroll = 2;      // 512-element steps per quantisation unit

@@ -90,6 +90,7 @@ def _load() -> ctypes.CDLL:
         "ep_convert_combine_input": (S, [P, P, P, P]),
         "ep_sync": (S, [P, P]),
         "ep_last_error": (ctypes.c_char_p, []),
+        "ep_routing_layout_noalloc": (S, [I, I, I, I, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -179,6 +180,17 @@ def ep_sync(handle, stream) -> None:
 
 def ep_last_error() -> str:
     return _lib.ep_last_error().decode()
+
+
+def ep_routing_layout_noalloc(world_size, max_num_inp_token_per_rank, num_experts_per_rank,
+                              num_experts_per_token, indices, num_tokens, recv_num_token,
+                              src_token_pos, slot_map, error_flags, stream) -> None:
+    """Routing layout with the library's static scratch (no device allocation)."""
+    nt = (ctypes.c_int32 * len(num_tokens))(*[int(n) for n in num_tokens])
+    _check(_lib.ep_routing_layout_noalloc(world_size, max_num_inp_token_per_rank,
+                                          num_experts_per_rank, num_experts_per_token, indices,
+                                          nt, recv_num_token, src_token_pos, slot_map,
+                                          error_flags, stream))
 
 
 # ------------------------------------------------------- operator class

@@ -250,6 +250,39 @@ ep_status ep_sync(ep_handle* h, void* stream);
 /* (+) Message for the calling thread's last failed call ("" if none). */
 const char* ep_last_error(void);
 
+/*
+ * Routing layout with no device allocation. The pages have no counterpart:
+ * this is the layout half of dispatch on its own, for callers that cannot
+ * call cudaMalloc -- plugins and embedded engines whose host application has
+ * reserved all device memory in its own pool (one more allocation fails or
+ * fragments it), and code paths that must not enter a device allocator. It
+ * allocates nothing (no cudaMalloc/cudaFree, no allocating library call):
+ * its scratch is one static device array of EP_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until the process exits.
+ *   indices         device [R][Tmax][k] int32 in [-1, R*E_r)
+ *   num_tokens      host [R], each <= Tmax
+ *   recv_num_token  device [R] out
+ *   src_token_pos   device [R][R*Tmax] out (first recv_num_token[r] rows written)
+ *   slot_map        device [R][Tmax][R] out: receive row of token (s,t) on rank r, or -1
+ *                   (tokens past num_tokens untouched)
+ *   error_flags     device int32 out or NULL: nonzero if an expert id outside
+ *                   [-1, E) was skipped
+ * Results equal those of ep_dispatch (same kernel, same order). Limit:
+ * world_size * Tmax <= EP_NOALLOC_MAX_TOKENS, else EP_ERR_INVALID_ARG with a
+ * message. The first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture. Every call shares the array and it keeps the last
+ * call's contents; each call clears what must start at zero. Calls that
+ * overlap on the GPU race on the array: serialise them.
+ */
+#define EP_NOALLOC_MAX_TOKENS 65536
+#define EP_NOALLOC_SCRATCH_BYTES 2433280
+ep_status ep_routing_layout_noalloc(int32_t world_size, int32_t max_num_inp_token_per_rank,
+                                    int32_t num_experts_per_rank, int32_t num_experts_per_token,
+                                    const int32_t* indices, const int32_t* num_tokens,
+                                    int32_t* recv_num_token, int32_t* src_token_pos,
+                                    int32_t* slot_map, int32_t* error_flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
