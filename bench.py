@@ -172,7 +172,9 @@ class Step:
         self.x = make_tokens(wl, seed, device=device)
         self.idx = torch.from_numpy(make_indices(wl, seed)).to(device)
         self.w = torch.from_numpy(make_weights(wl, seed)).to(device)
+        from combine_route_layout_gb300 import ep as _ep
         self.ntok = make_num_tokens(wl)
+        self.ntok_c = _ep._i32_array(self.ntok)
         R, T = wl.world_size, wl.tokens_per_rank
         if wl.standard_moe:
             v = self.op.dispatch_standard_moe(self.x, self.w, None, self.idx, self.ntok)
@@ -203,8 +205,8 @@ class Step:
         w = self.w if w is None else w
         idx = self.idx if idx is None else idx
         if self.wl.standard_moe:
-            return self.op.dispatch_standard_moe(x, w, None, idx, self.ntok)
-        return self.op.dispatch(x, w, None, idx, self.ntok)
+            return self.op.dispatch_standard_moe(x, w, None, idx, self.ntok_c)
+        return self.op.dispatch(x, w, None, idx, self.ntok_c)
 
     def combine(self, d, y=None, w=None):
         y = self.y if y is None else y
@@ -224,12 +226,16 @@ def time_steps(step: Step, K: int, W: int, flush: torch.Tensor | None, dist_barr
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    flush_sink = torch.empty((), dtype=torch.float32, device=step.dev) if flush is not None else None
     dist_barrier()
     torch.cuda.synchronize()
     t0.record(st)
     for i in range(K):
         if flush is not None:
-            flush.add_(1)              # evict L2 between iterations (outside the kernel events)
+            # evict L2 between iterations (outside the kernel events) by reading a
+            # buffer twice its size: a read leaves clean lines, so the timed kernels
+            # pay no write-back for it
+            torch.sum(flush, dim=0, out=flush_sink)
         ev[i][0].record(st)
         d = step.dispatch()
         ev[i][1].record(st)
@@ -242,6 +248,32 @@ def time_steps(step: Step, K: int, W: int, flush: torch.Tensor | None, dist_barr
     disp = [e[0].elapsed_time(e[1]) for e in ev]
     comb = [e[1].elapsed_time(e[2]) for e in ev]
     return total_ms, disp, comb
+
+
+def graph_step_times(step: Step, iters: int, flush: torch.Tensor):
+    """Dispatch + combine captured once into a CUDA graph and replayed, with an
+    L2-evicting read before each replay; returns per-replay device times (µs)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step.combine(step.dispatch())
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.combine(step.dispatch())
+    sink = torch.empty((), dtype=torch.float32, device=step.dev)
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for i in range(iters):
+        torch.sum(flush, dim=0, out=sink)
+        ev[i][0].record(st)
+        g.replay()
+        ev[i][1].record(st)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
 
 
 def time_e2e(step: Step, K: int, W: int, dist_barrier):
@@ -494,16 +526,20 @@ def main():
     if not args.no_latency and rank == 0:
         lw = WORKLOADS[args.latency_workload]
         ls = Step(lw, dev)
-        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         lk = max(50, K)
         _, ld, lc = time_steps(ls, lk, max(args.warmup, 5), flush, lambda: None)
         lb = ls.bytes
+        graph_us = graph_step_times(ls, lk, flush)
         line["latency_shape"] = {
-            "workload": lw.name, "iters": lk, "l2": "flushed (256 MB write) before each step",
+            "workload": lw.name, "iters": lk, "l2": "flushed (256 MB read) before each step",
             "dispatch_us_median": round(statistics.median(ld) * 1e3, 2),
             "combine_us_median": round(statistics.median(lc) * 1e3, 2),
             "dispatch_GBps": round(lb["dispatch"] / (statistics.median(ld) * 1e-3) / 1e9, 1),
             "combine_GBps": round(lb["combine"] / (statistics.median(lc) * 1e-3) / 1e9, 1),
+            "graph_step_us": round(statistics.median(graph_us), 2),
+            "graph_step_GBps": round((lb["dispatch"] + lb["combine"])
+                                     / (statistics.median(graph_us) * 1e-6) / 1e9, 1),
         }
         del ls, flush
 

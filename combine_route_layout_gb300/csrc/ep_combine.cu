@@ -231,15 +231,17 @@ template <template <int, int, int> class KSel, int MAXD_SMALL>
 cudaError_t launch_combine(const CombineParams& p, int in_dtype, int out_dtype, bool small,
                            const LaunchCfg& lc, cudaStream_t st) {
   if (p.total_units == 0) return cudaSuccess;
+  cudaError_t err = cudaSuccess;
   auto go = [&](auto kernel) {
     kernel<<<auto_grid(kernel, lc, p.total_units), lc.block, 0, st>>>(p);
+    err = cudaGetLastError();
   };
   const bool ib = in_dtype == EP_DTYPE_BF16, ob = out_dtype == EP_DTYPE_BF16;
   if (ib && ob) small ? go(KSel<EP_DTYPE_BF16, EP_DTYPE_BF16, MAXD_SMALL>::fn) : go(KSel<EP_DTYPE_BF16, EP_DTYPE_BF16, 0>::fn);
   else if (ib) small ? go(KSel<EP_DTYPE_BF16, EP_DTYPE_FP32, MAXD_SMALL>::fn) : go(KSel<EP_DTYPE_BF16, EP_DTYPE_FP32, 0>::fn);
   else if (ob) small ? go(KSel<EP_DTYPE_FP32, EP_DTYPE_BF16, MAXD_SMALL>::fn) : go(KSel<EP_DTYPE_FP32, EP_DTYPE_BF16, 0>::fn);
   else small ? go(KSel<EP_DTYPE_FP32, EP_DTYPE_FP32, MAXD_SMALL>::fn) : go(KSel<EP_DTYPE_FP32, EP_DTYPE_FP32, 0>::fn);
-  return cudaGetLastError();
+  return err;
 }
 
 template <int IN, int OUT, int MAXD>

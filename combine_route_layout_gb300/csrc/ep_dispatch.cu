@@ -98,9 +98,10 @@ __device__ void write_meta_std(const DispatchParams& p, int64_t g, int s, int t,
 // Payload bits are moved unchanged: lane covers 16 bytes per 512-byte step.
 
 template <bool STD>
-__global__ void __launch_bounds__(256) dispatch_copy_kernel(DispatchParams p) {
+__global__ void __launch_bounds__(256, 4) dispatch_copy_kernel(DispatchParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  bool waited = false;
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
        u += nwarps) {
     const int64_t g = u / p.segs_per_token;
@@ -114,6 +115,10 @@ __global__ void __launch_bounds__(256) dispatch_copy_kernel(DispatchParams p) {
     for (int i = 0; i < kCopyUnroll; ++i) {
       const int64_t off = ((int64_t)seg * kCopyUnroll + i) * 512 + lane * 16;
       if (off < p.in_row_bytes) v[i] = ld_nc_v4(src + off);
+    }
+    if (!waited) {  // the routing layout is complete and visible past this point
+      pdl_wait();
+      waited = true;
     }
 
     if (!STD) {
@@ -145,12 +150,30 @@ __global__ void __launch_bounds__(256) dispatch_copy_kernel(DispatchParams p) {
       }
     }
   }
+  pdl_wait();  // never finish before the routing layout, even with no work
 }
 
 // ------------------------------------------------------------ FP8 quant mode
 // bf16 in. Lane covers 16 consecutive elements (two 16-byte loads) per
 // 512-element step, so 8 lanes cover one 128-element block; the block's amax
 // is reduced with three xor-shuffles inside that 8-lane group.
+
+// E4M3 codes of RN_f32(x0 / s) and RN_f32(x1 / s), bit-identical to dividing.
+// q = x * RN(1/s) carries two roundings, so |q - x/s| < 2 ulp(x/s) and q lies
+// within 3 units in the last place (counted on the f32 bit pattern) of
+// RN_f32(x/s). E4M3 rounding is monotone, so when q - 3 ulp and q + 3 ulp
+// convert to the same code, every value between them -- RN_f32(x/s)
+// included -- converts to that code. Otherwise (a code boundary within
+// 3 ulp, about 6 in 10^6 elements, or a pattern that wraps near zero) the
+// IEEE division is taken.
+__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float x0, float x1, float s, float r) {
+  const float q0 = __fmul_rn(x0, r), q1 = __fmul_rn(x1, r);
+  const uint32_t b0 = __float_as_uint(q0), b1 = __float_as_uint(q1);
+  const uint32_t lo = cvt_e4m3x2(__uint_as_float(b0 - 3u), __uint_as_float(b1 - 3u));
+  const uint32_t hi = cvt_e4m3x2(__uint_as_float(b0 + 3u), __uint_as_float(b1 + 3u));
+  if (lo == hi) return lo;
+  return cvt_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+}
 
 __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q, float& scale) {
   float f[16];
@@ -172,9 +195,9 @@ __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = cvt_e4m3x2(f[2 * i], f[2 * i + 1]);
   } else {
+    const float r = __frcp_rn(scale);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+    for (int i = 0; i < 8; ++i) c[i] = e4m3x2_of_quotients(f[2 * i], f[2 * i + 1], scale, r);
   }
   q.x = c[0] | (c[1] << 16);
   q.y = c[2] | (c[3] << 16);
@@ -183,10 +206,11 @@ __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q
 }
 
 template <bool STD>
-__global__ void __launch_bounds__(256) dispatch_quant_kernel(DispatchParams p) {
+__global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p) {
   const int lane = threadIdx.x & 31;
   const int nb = p.H / 128;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  bool waited = false;
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
        u += nwarps) {
     const int64_t g = u / p.segs_per_token;
@@ -211,6 +235,10 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(DispatchParams p) {
     float sc[kQuantUnroll];
 #pragma unroll
     for (int i = 0; i < kQuantUnroll; ++i) quant16(a[i], b[i], q[i], sc[i]);
+    if (!waited) {  // the routing layout is complete and visible past this point
+      pdl_wait();
+      waited = true;
+    }
 
     // Each destination row gets the codes and the block scales.
     auto put = [&](int64_t row) {
@@ -243,20 +271,15 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(DispatchParams p) {
       }
     }
   }
+  pdl_wait();  // never finish before the routing layout, even with no work
 }
 
 template <bool STD>
 cudaError_t launch_dispatch(const DispatchParams& p, bool quant, const LaunchCfg& lc,
                             cudaStream_t st) {
   if (p.total_units == 0) return cudaSuccess;
-  if (quant) {
-    auto k = dispatch_quant_kernel<STD>;
-    k<<<auto_grid(k, lc, p.total_units), lc.block, 0, st>>>(p);
-  } else {
-    auto k = dispatch_copy_kernel<STD>;
-    k<<<auto_grid(k, lc, p.total_units), lc.block, 0, st>>>(p);
-  }
-  return cudaGetLastError();
+  auto k = quant ? dispatch_quant_kernel<STD> : dispatch_copy_kernel<STD>;
+  return launch_pdl(k, auto_grid(k, lc, p.total_units), lc.block, 0, st, p);
 }
 
 }  // namespace

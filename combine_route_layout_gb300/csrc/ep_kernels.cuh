@@ -175,7 +175,29 @@ ep_status record_error(ep_status st, const char* msg);
 // Work-unit geometry used by the launchers and the host library alike.
 constexpr int kCopyUnroll = 4;       // 16-byte vectors per lane per copy unit
 constexpr int kQuantUnroll = 2;      // 512-element steps per quantisation unit
-constexpr int kCombineUnroll = 2;    // 256-element steps per combine unit
+#ifndef EP_COMBINE_UNROLL
+#define EP_COMBINE_UNROLL 2
+#endif
+constexpr int kCombineUnroll = EP_COMBINE_UNROLL;  // 256-element steps per combine unit
+
+// Launch `kernel` with programmatic stream serialization, so it may begin
+// while the previous kernel in the stream is still running (it waits with
+// griddepcontrol.wait before reading that kernel's outputs).
+template <typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 }  // namespace ep
 
@@ -222,6 +244,15 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Programmatic dependent launch: let the next kernel in the stream start
+// (it must call pdl_wait before touching this kernel's outputs) ...
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, in that next kernel, wait until the previous grid has finished and
+// its writes are visible. A no-op when the kernel was launched without PDL.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;

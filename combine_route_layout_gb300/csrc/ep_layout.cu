@@ -25,34 +25,6 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kWarps = kLayoutThreads / 32;
 
-// Exclusive scan of one int per thread across the CTA; *total gets the sum.
-__device__ int cta_exclusive_scan(int v, int* sm, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sm[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? sm[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += y;
-    }
-    sm[lane] = w;
-  }
-  __syncthreads();
-  const int before = warp ? sm[warp - 1] : 0;
-  *total = sm[nw - 1];
-  __syncthreads();
-  return before + x - v;
-}
-
 // Release this CTA's global writes and report whether it finished last.
 __device__ bool elect_last_cta(unsigned int* ticket) {
   __shared__ bool last;
@@ -65,9 +37,9 @@ __device__ bool elect_last_cta(unsigned int* ticket) {
 }
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_2d_kernel(LayoutParams p) {
+  pdl_launch_dependents();  // the dispatch kernel may start its independent loads now
   __shared__ int wcnt[kWarps][EP_MAX_WORLD_SIZE];
   __shared__ int wpre[kWarps][EP_MAX_WORLD_SIZE];
-  __shared__ int scan_sm[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x;
   const int s = c / p.cpr;
@@ -112,26 +84,34 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_2d_kernel(LayoutParams 
   }
 
   if (!elect_last_cta(p.ticket)) return;
-  // Last CTA: per destination rank, exclusive scan of the chunk counts.
-  const int per = (p.nchunks + blockDim.x - 1) / blockDim.x;
-  const int c0 = threadIdx.x * per;
-  const int c1 = min(c0 + per, p.nchunks);
-  for (int r = 0; r < p.R; ++r) {
+  // Last CTA: one warp per destination rank scans that rank's chunk counts
+  // (each lane a contiguous run of chunks), all ranks in parallel.
+  const int32_t* __restrict__ cnt = p.chunk_cnt;
+  int32_t* __restrict__ off = p.chunk_off;
+  const int per = (p.nchunks + 31) / 32;
+  for (int r = warp; r < p.R; r += kWarps) {
+    const int c0 = min(lane * per, p.nchunks), c1 = min(c0 + per, p.nchunks);
     int sum = 0;
-    for (int cc = c0; cc < c1; ++cc) sum += __ldcg(p.chunk_cnt + (int64_t)cc * p.R + r);
-    int total;
-    int ex = cta_exclusive_scan(sum, scan_sm, &total);
+    for (int cc = c0; cc < c1; ++cc) sum += __ldcg(cnt + (int64_t)cc * p.R + r);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int ex = incl - sum;
     for (int cc = c0; cc < c1; ++cc) {
-      const int v = __ldcg(p.chunk_cnt + (int64_t)cc * p.R + r);
-      p.chunk_off[(int64_t)cc * p.R + r] = ex;
+      const int v = __ldcg(cnt + (int64_t)cc * p.R + r);
+      off[(int64_t)cc * p.R + r] = ex;
       ex += v;
     }
-    if (threadIdx.x == 0) p.recv_num_token[r] = total;
+    if (lane == 31) p.recv_num_token[r] = incl;
   }
   if (threadIdx.x == 0) *p.ticket = 0u;
 }
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams p) {
+  pdl_launch_dependents();
   // bits[w][e]: lanes of warp w whose token selects expert e; pre[w][e]: rows of
   // expert e from warps before w in this chunk.
   extern __shared__ uint32_t dyn[];
@@ -188,16 +168,23 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
   if (!elect_last_cta(p.ticket)) return;
   // Last CTA: per expert, scan over chunks (grouped by source rank), then the
   // padded segment offsets per destination rank and the padding rows.
+  const int32_t* __restrict__ cnt = p.chunk_cnt;
+  int32_t* __restrict__ coff = p.chunk_off;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     const int r = e / p.E_r, el = e % p.E_r;
     int run = 0;
     for (int src = 0; src < p.R; ++src) {
       const int begin = run;
-      for (int cc = 0; cc < p.cpr; ++cc) {
-        const int64_t ci = (int64_t)(src * p.cpr + cc) * p.E + e;
-        const int v = __ldcg(p.chunk_cnt + ci);
-        p.chunk_off[ci] = run;
-        run += v;
+      for (int cc0 = 0; cc0 < p.cpr; cc0 += 8) {   // 8 independent loads, then the stores
+        int v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          v[q] = cc0 + q < p.cpr ? __ldcg(cnt + (int64_t)(src * p.cpr + cc0 + q) * p.E + e) : 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (cc0 + q < p.cpr) coff[(int64_t)(src * p.cpr + cc0 + q) * p.E + e] = run;
+          run += v[q];
+        }
       }
       p.layout_range[((int64_t)r * p.E_r + el) * p.R + src] =
           (int64_t)(((uint64_t)(uint32_t)begin << 32) | (uint32_t)(run - begin));

@@ -127,10 +127,16 @@ def ep_destroy(handle: int) -> None:
     _lib.ep_destroy(handle)
 
 
+def _i32_array(values):
+    if isinstance(values, ctypes.Array):
+        return values
+    return (ctypes.c_int32 * len(values))(*[int(n) for n in values])
+
+
 def ep_dispatch(handle, x, weights, scales, indices, num_tokens, stream) -> ep_dispatch_out:
     out = ep_dispatch_out()
-    nt = (ctypes.c_int32 * len(num_tokens))(*[int(n) for n in num_tokens])
-    _check(_lib.ep_dispatch(handle, x, weights, scales, indices, nt, stream, ctypes.byref(out)))
+    _check(_lib.ep_dispatch(handle, x, weights, scales, indices, _i32_array(num_tokens), stream,
+                            ctypes.byref(out)))
     return out
 
 
@@ -152,9 +158,8 @@ def ep_reset(handle, stream=None) -> None:
 def ep_dispatch_standard_moe(handle, x, weights, scales, indices, num_tokens,
                              stream) -> ep_std_moe_out:
     out = ep_std_moe_out()
-    nt = (ctypes.c_int32 * len(num_tokens))(*[int(n) for n in num_tokens])
-    _check(_lib.ep_dispatch_standard_moe(handle, x, weights, scales, indices, nt, stream,
-                                         ctypes.byref(out)))
+    _check(_lib.ep_dispatch_standard_moe(handle, x, weights, scales, indices,
+                                         _i32_array(num_tokens), stream, ctypes.byref(out)))
     return out
 
 
@@ -270,8 +275,10 @@ class EpDispatchCombineOp:
         return self.workspace[off:off + nbytes].view(dtype).view(*shape)
 
     def _num_tokens(self, num_tokens):
-        R, T = self.config.world_size, self.config.max_num_inp_token_per_rank
-        return [T] * R if num_tokens is None else [int(n) for n in num_tokens]
+        if num_tokens is None:
+            R, T = self.config.world_size, self.config.max_num_inp_token_per_rank
+            return [T] * R
+        return num_tokens
 
     @property
     def _dispatch_dtype(self):
@@ -283,10 +290,18 @@ class EpDispatchCombineOp:
 
     # section 3 ----------------------------------------------------------------
     def dispatch(self, input, weights, scales, indices, num_tokens=None):
-        cfg = self.config
-        R, H, k = cfg.world_size, cfg.hidden_dim, cfg.num_experts_per_token
         o = ep_dispatch(self._handle, _ptr(input), _ptr(weights), _ptr(scales), _ptr(indices),
                         self._num_tokens(num_tokens), _stream())
+        # the outputs always live at the same workspace offsets: build the views once
+        key = (o.x, o.scales, o.weights, o.indices, o.recv_num_token)
+        if getattr(self, "_dispatch_key", None) != key:
+            self._dispatch_views = self._make_dispatch_views(o)
+            self._dispatch_key = key
+        return self._dispatch_views
+
+    def _make_dispatch_views(self, o):
+        cfg = self.config
+        R, H, k = cfg.world_size, cfg.hidden_dim, cfg.num_experts_per_token
         x = self._view(o.x, self._dispatch_dtype, (R, self.cap, H))
         if o.scales:
             if cfg.quant_type != "none":

@@ -471,3 +471,46 @@ def test_cuda_graph_capture_replay():
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+def test_fp8_quotients_on_e4m3_midpoints():
+    """Blocks whose amax is 448*c (so the scale is exactly c) and whose other
+    elements are c times an E4M3 midpoint (or one bf16 step away): x / scale
+    lands exactly on a rounding boundary, where the reciprocal-multiply fast
+    path must hand over to the IEEE division. Codes must still match the
+    oracle bit for bit."""
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=48, hidden=1024)
+    R, T, H = wl.world_size, wl.tokens_per_rank, wl.hidden
+    codes = np.array([c for c in range(0x7F) if c != 0x7F], np.uint8)
+    vals = oracle.e4m3_to_f32(codes).astype(np.float64)
+    mids = np.concatenate([(vals[1:] + vals[:-1]) / 2, vals])
+    mults = np.array([3, 5, 7, 0.75, 1.5, 2.5, 3.5, 0.375, 1.25, 96, 0.0234375, 6], np.float64)
+    rng = np.random.default_rng(11)
+    x = np.empty((R, T, H), np.float32)
+    for s in range(R):
+        for t in range(T):
+            for b in range(H // 128):
+                c = mults[rng.integers(len(mults))]
+                blk = c * rng.choice(mids, size=128) * rng.choice([-1.0, 1.0], size=128)
+                blk[rng.integers(128)] = 448.0 * c * rng.choice([-1.0, 1.0])
+                x[s, t, b * 128:(b + 1) * 128] = blk
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    nudge = rng.random(xb.shape) < 0.2          # some elements one bf16 step off the midpoint
+    xi = xb.view(torch.int16)
+    xi[torch.from_numpy(nudge)] += torch.from_numpy(rng.choice([-1, 1], size=int(nudge.sum()))
+                                                    ).to(torch.int16)
+    inp = Inputs(wl, 0)
+    inp.x = xb.to(DEV)
+    cfg = make_config(wl)
+    op = EpDispatchCombineOp(cfg)
+    d_x, d_w, d_sc, _, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    q, sc = oracle.quant_tokens(bits16(xb))
+    x_ref, sc_ref = oracle.place_rows(q, inp.ntok, slot), oracle.place_rows(sc, inp.ntok, slot)
+    gx, gsc = host(d_x), host(d_sc)
+    for r in range(R):
+        n = recv[r]
+        assert np.array_equal(gsc[r, :n].view(np.uint32), sc_ref[r, :n].view(np.uint32))
+        assert np.array_equal(gx[r, :n], x_ref[r, :n]), f"codes rank {r}"
+    op.reset()
