@@ -148,6 +148,10 @@ class ClockSampler:
 
 # ---------------------------------------------------------- our arm
 
+COMBINE_IMPL = "auto"
+DISPATCH_IMPL = "auto"
+
+
 def make_op(wl, device):
     from combine_route_layout_gb300 import EpDispatchCombineConfig, EpDispatchCombineOp
     cfg = EpDispatchCombineConfig(
@@ -158,7 +162,8 @@ def make_op(wl, device):
         quant_type="fp8_e4m3_block128" if wl.dispatch_dtype == "fp8" else "none",
         combine_dtype=torch.bfloat16,
         combine_out_dtype=torch.float32 if wl.combine_out_dtype == "fp32" else torch.bfloat16,
-        weighted_combine=wl.weighted, standard_moe=wl.standard_moe)
+        weighted_combine=wl.weighted, standard_moe=wl.standard_moe, combine_impl=COMBINE_IMPL,
+        dispatch_impl=DISPATCH_IMPL)
     return EpDispatchCombineOp(cfg, device)
 
 
@@ -448,6 +453,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ds_v3_throughput", choices=sorted(WORKLOADS))
     ap.add_argument("--latency-workload", default="ds_v3_latency")
+    ap.add_argument("--combine-impl", default="auto", choices=["auto", "vector", "bulk"])
+    ap.add_argument("--dispatch-impl", default="auto", choices=["auto", "vector", "bulk"])
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override the workload's tokens per rank (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -462,6 +469,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    global COMBINE_IMPL, DISPATCH_IMPL
+    COMBINE_IMPL = args.combine_impl
+    DISPATCH_IMPL = args.dispatch_impl
     rank, world, local = dist_setup(args.gpus)
     wl = WORKLOADS[args.workload]
     if args.tokens_per_rank > 0:
@@ -494,8 +504,18 @@ def main():
     dom = "combine" if c_mean >= d_mean else "dispatch"
     dom_key = {"combine": "combine_2d" if not wl.standard_moe else "combine_std",
                "dispatch": "dispatch_2d" if not wl.standard_moe else "dispatch_std"}[dom]
+    # the kernel the library runs for that step (its EP_COMBINE_AUTO rule: bulk copies
+    # for the 2D layout from 8192 source tokens and up to 8 ranks)
+    bulk = (COMBINE_IMPL == "bulk" or (COMBINE_IMPL == "auto" and step.Ttot >= 8192)) \
+        and wl.world_size <= 8 and not wl.standard_moe
+    dom_kernel = {"combine": "combine_bulk_kernel" if bulk else
+                  ("combine_std_kernel" if wl.standard_moe else "combine_2d_kernel"),
+                  "dispatch": "dispatch_quant_kernel" if wl.dispatch_dtype == "fp8"
+                  else "dispatch_copy_kernel"}[dom]
     ach = c_gbs if dom == "combine" else d_gbs
     tr = profiled_traffic(dom_key)
+    if tr and not tr["kernel"].startswith(dom_kernel.replace("_kernel", "")):
+        tr = None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(per_step, 4),
@@ -514,7 +534,7 @@ def main():
         "combine": {"us_median": round(c_us, 2), "us_mean": round(c_mean, 2),
                     "bytes": b["combine"], "GBps": round(c_gbs, 1),
                     "frac_of_peak": round(c_gbs / peak, 4)},
-        "roofline": {"bound": "hbm", "kernel": dom_key, "achieved": round(ach, 1),
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(ach, 1),
                      "peak": peak, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(ach / peak, 4),

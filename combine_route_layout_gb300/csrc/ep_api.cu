@@ -33,6 +33,10 @@ ep_status cuda_fail(cudaError_t e, const char* what) {
 
 enum State { kReady = 0, kDispatched = 1, kCombined = 2 };
 
+
+// EP_COMBINE_AUTO picks the bulk-copy combine from this many source tokens on.
+constexpr int64_t kBulkMinTokens = 8192;
+
 int dtype_size(int dt) {
   switch (dt) {
     case EP_DTYPE_BF16: return 2;
@@ -51,7 +55,8 @@ struct Geometry {
   int R, H, k, E_r, E, Tmax;
   int64_t cap, pcap;
   int cpr, nchunks, cpr_recv, nchunks_recv;
-  bool quant, std_moe;
+  bool quant, std_moe, registered_in;
+  int64_t combine_in_row_bytes;
   int64_t in_row_bytes, out_row_bytes;
   int scale_row_bytes;       // received scale row bytes (0 = none)
   int in_scale_row_bytes;    // pass-through input scale row bytes
@@ -86,6 +91,7 @@ struct Carve {
   uint16_t* conv_local16;
   int32_t* conv_chunk_cnt;
   int32_t* conv_chunk_off;
+  uint8_t* reg_combine_in;   // registered combine input [R][cap][H] (zero-copy mode)
   size_t total;
 };
 
@@ -128,6 +134,7 @@ Carve carve(const Geometry& g, uint8_t* base) {
     take(base, off, c.conv_chunk_cnt, (size_t)g.nchunks_recv * g.E_r * 4);
     take(base, off, c.conv_chunk_off, (size_t)g.nchunks_recv * g.E_r * 4);
   }
+  if (g.registered_in) take(base, off, c.reg_combine_in, R * g.cap * g.combine_in_row_bytes);
   c.total = off;
   return c;
 }
@@ -162,6 +169,10 @@ ep_status make_geometry(const ep_config* cfg, Geometry* g) {
     return fail(EP_ERR_INVALID_ARG, "scale_type_size must be 1, 2, 4 or 8");
   if (cfg->warp_num_per_block > 8)
     return fail(EP_ERR_INVALID_ARG, "warp_num_per_block must be <= 8");
+  if (cfg->combine_impl < EP_COMBINE_AUTO || cfg->combine_impl > EP_COMBINE_BULK)
+    return fail(EP_ERR_INVALID_ARG, "unknown combine_impl %d", cfg->combine_impl);
+  if (cfg->dispatch_impl < EP_DISPATCH_AUTO || cfg->dispatch_impl > EP_DISPATCH_BULK)
+    return fail(EP_ERR_INVALID_ARG, "unknown dispatch_impl %d", cfg->dispatch_impl);
   Geometry x{};
   x.R = R; x.H = H; x.k = k; x.E_r = E_r; x.E = R * E_r; x.Tmax = T;
   x.cap = (int64_t)R * T;
@@ -171,6 +182,8 @@ ep_status make_geometry(const ep_config* cfg, Geometry* g) {
   x.nchunks_recv = R * x.cpr_recv;
   x.quant = quant;
   x.std_moe = cfg->standard_moe != 0;
+  x.registered_in = cfg->use_external_inp_buf == 0;
+  x.combine_in_row_bytes = (int64_t)H * dtype_size(cfg->combine_dtype);
   x.in_row_bytes = (int64_t)H * in_sz;
   if (x.in_row_bytes % 16 != 0)
     return fail(EP_ERR_INVALID_ARG, "hidden_dim * element size must be a multiple of 16 bytes");
@@ -261,6 +274,31 @@ ep::LaunchCfg launch_cfg(const ep_handle* h) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Bulk-copy combine when asked for, or under EP_COMBINE_AUTO when it measured
+// faster on GB300: the 2D layout with at least kBulkMinTokens source tokens
+// (its four-stage ring needs several tokens per CTA to stay full; with fewer,
+// and for the packed layout, the vector kernel was as fast or faster).
+bool use_bulk(const ep_handle* h, const ep::CombineParams& p, bool std_layout) {
+  if (h->cfg.combine_impl == EP_COMBINE_VECTOR) return false;
+  if (!ep::combine_bulk_supported(p, std_layout)) return false;
+  if (h->cfg.combine_impl == EP_COMBINE_BULK) return true;
+  int64_t tokens = 0;
+  for (int r = 0; r < h->g.R; ++r) tokens += h->ntok[r];
+  return !std_layout && tokens >= kBulkMinTokens;
+}
+
+// Bulk-copy dispatch (copy mode only) when asked for, or under
+// EP_DISPATCH_AUTO from kBulkMinTokens source tokens on (measured slightly
+// faster there on GB300, slower for a handful of tokens).
+bool use_bulk_dispatch(const ep_handle* h, const ep::DispatchParams& p) {
+  if (h->g.quant || h->cfg.dispatch_impl == EP_DISPATCH_VECTOR) return false;
+  if (!ep::dispatch_bulk_supported(p)) return false;
+  if (h->cfg.dispatch_impl == EP_DISPATCH_BULK) return true;
+  int64_t tokens = 0;
+  for (int r = 0; r < h->g.R; ++r) tokens += h->ntok[r];
+  return tokens >= kBulkMinTokens;
+}
 
 ep_status check_tokens(ep_handle* h, const int32_t* num_tokens) {
   if (!num_tokens) return fail(EP_ERR_INVALID_ARG, "num_tokens is NULL");
@@ -392,7 +430,9 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
   dp.out_scales = h->w.recv_scales;
   dp.out_w = h->w.recv_w;
   dp.out_idx = h->w.recv_idx;
-  e = ep::launch_dispatch_2d(dp, h->g.quant, launch_cfg(h), st);
+  dp.err = h->w.err;
+  e = use_bulk_dispatch(h, dp) ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h), st)
+                               : ep::launch_dispatch_2d(dp, h->g.quant, launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
 
   h->state = kDispatched;
@@ -418,7 +458,10 @@ ep_status ep_combine(ep_handle* h, const void* expert_out, const float* weights,
   (void)indices;
   if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
   if (!h->has2d || h->state == kReady) return fail(EP_ERR_STATE, "combine needs a preceding dispatch");
-  if (!expert_out || !out) return fail(EP_ERR_INVALID_ARG, "expert_out and out must be non-NULL");
+  if (!expert_out) expert_out = h->w.reg_combine_in;  // zero-copy mode
+  if (!expert_out || !out)
+    return fail(EP_ERR_INVALID_ARG,
+                "out must be non-NULL, and expert_out too unless use_external_inp_buf = 0");
   if (!aligned(expert_out, 16) || !aligned(out, 16))
     return fail(EP_ERR_INVALID_ARG, "expert_out and out must be 16-byte aligned");
   if ((h->cfg.weighted_combine || out_weights) && !weights)
@@ -441,11 +484,23 @@ ep_status ep_combine(ep_handle* h, const void* expert_out, const float* weights,
   p.slot_map = h->w.slot_map;
   p.out = static_cast<uint8_t*>(out);
   p.out_w = out_weights;
-  cudaError_t e = ep::launch_combine_2d(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
-                                        launch_cfg(h), st);
+  p.err = h->w.err;
+  cudaError_t e = use_bulk(h, p, false)
+                      ? ep::launch_combine_2d_bulk(p, h->cfg.combine_dtype,
+                                                   h->cfg.combine_out_dtype, launch_cfg(h), st)
+                      : ep::launch_combine_2d(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
+                                              launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   h->state = kCombined;
   if (call_reset) return ep_reset(h, stream);
+  return EP_OK;
+}
+
+ep_status ep_get_registered_combine_input_buffer(ep_handle* h, void** d_buffer) {
+  if (!h || !d_buffer) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+  if (!h->w.reg_combine_in)
+    return fail(EP_ERR_STATE, "config has use_external_inp_buf != 0: no registered buffer");
+  *d_buffer = h->w.reg_combine_in;
   return EP_OK;
 }
 
@@ -503,7 +558,9 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
   dp.row_map = h->w.row_map;
   dp.out_x = h->w.packed_x;
   dp.out_scales = h->w.packed_scales;
-  e = ep::launch_dispatch_std(dp, h->g.quant, launch_cfg(h), st);
+  dp.err = h->w.err;
+  e = use_bulk_dispatch(h, dp) ? ep::launch_dispatch_bulk_copy(dp, true, launch_cfg(h), st)
+                               : ep::launch_dispatch_std(dp, h->g.quant, launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "standard-MoE dispatch launch");
 
   h->state = kDispatched;
@@ -551,8 +608,12 @@ ep_status ep_combine_standard_moe(ep_handle* h, const void* expert_out, const fl
   p.w = weights;
   p.row_map = h->w.row_map;
   p.out = static_cast<uint8_t*>(out);
-  cudaError_t e = ep::launch_combine_std(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
-                                         launch_cfg(h), st);
+  p.err = h->w.err;
+  cudaError_t e = use_bulk(h, p, true)
+                      ? ep::launch_combine_std_bulk(p, h->cfg.combine_dtype,
+                                                    h->cfg.combine_out_dtype, launch_cfg(h), st)
+                      : ep::launch_combine_std(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
+                                               launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "standard-MoE combine launch");
   h->state = kCombined;
   if (call_reset) return ep_reset(h, stream);
@@ -668,6 +729,8 @@ ep_status ep_sync(ep_handle* h, void* stream) {
   e = cudaMemsetAsync(h->w.err, 0, sizeof(int32_t), st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the error flags");
+  if (bits & ep::kErrTimeout)
+    return fail(EP_ERR_TIMEOUT, "a kernel's bounded wait on a shared-memory barrier gave up");
   if (bits & (ep::kErrIndex | ep::kErrDuplicate))
     return fail(EP_ERR_INVALID_INDEX, "an expert id was outside [-1, %d)%s", h->g.E,
                 (bits & ep::kErrDuplicate) ? " or repeated within a token (standard MoE)" : "");

@@ -78,11 +78,11 @@ __device__ __forceinline__ void store8(uint8_t* base, int64_t elem, const float 
     v.y = cvt_bf16x2(f[2], f[3]);
     v.z = cvt_bf16x2(f[4], f[5]);
     v.w = cvt_bf16x2(f[6], f[7]);
-    st_v4(base + elem * 2, v);
+    st_v4_cs(base + elem * 2, v);
   } else {
-    st_v4(base + elem * 4, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+    st_v4_cs(base + elem * 4, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
                                       __float_as_uint(f[2]), __float_as_uint(f[3])));
-    st_v4(base + elem * 4 + 16, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+    st_v4_cs(base + elem * 4 + 16, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
                                            __float_as_uint(f[6]), __float_as_uint(f[7])));
   }
 }

@@ -158,23 +158,6 @@ __global__ void __launch_bounds__(256, 4) dispatch_copy_kernel(DispatchParams p)
 // 512-element step, so 8 lanes cover one 128-element block; the block's amax
 // is reduced with three xor-shuffles inside that 8-lane group.
 
-// E4M3 codes of RN_f32(x0 / s) and RN_f32(x1 / s), bit-identical to dividing.
-// q = x * RN(1/s) carries two roundings, so |q - x/s| < 2 ulp(x/s) and q lies
-// within 3 units in the last place (counted on the f32 bit pattern) of
-// RN_f32(x/s). E4M3 rounding is monotone, so when q - 3 ulp and q + 3 ulp
-// convert to the same code, every value between them -- RN_f32(x/s)
-// included -- converts to that code. Otherwise (a code boundary within
-// 3 ulp, about 6 in 10^6 elements, or a pattern that wraps near zero) the
-// IEEE division is taken.
-__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float x0, float x1, float s, float r) {
-  const float q0 = __fmul_rn(x0, r), q1 = __fmul_rn(x1, r);
-  const uint32_t b0 = __float_as_uint(q0), b1 = __float_as_uint(q1);
-  const uint32_t lo = cvt_e4m3x2(__uint_as_float(b0 - 3u), __uint_as_float(b1 - 3u));
-  const uint32_t hi = cvt_e4m3x2(__uint_as_float(b0 + 3u), __uint_as_float(b1 + 3u));
-  if (lo == hi) return lo;
-  return cvt_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-}
-
 __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q, float& scale) {
   float f[16];
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -195,9 +178,9 @@ __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = cvt_e4m3x2(f[2 * i], f[2 * i + 1]);
   } else {
-    const float r = __frcp_rn(scale);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = e4m3x2_of_quotients(f[2 * i], f[2 * i + 1], scale, r);
+    for (int i = 0; i < 8; ++i)
+      c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
   }
   q.x = c[0] | (c[1] << 16);
   q.y = c[2] | (c[3] << 16);

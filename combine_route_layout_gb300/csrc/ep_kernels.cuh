@@ -18,6 +18,7 @@ constexpr int kPadRows = 128;        // standard-MoE segment alignment
 constexpr int kErrIndex = 1;      // expert id outside [-1, E)
 constexpr int kErrDuplicate = 2;  // repeated expert id in one token (standard MoE)
 constexpr int kErrCapacity = 4;   // packed rows beyond max_packed_rows_per_rank
+constexpr int kErrTimeout = 8;    // a bounded wait on an mbarrier gave up
 
 // ------------------------------------------------------------ parameter blocks
 
@@ -74,6 +75,7 @@ struct DispatchParams {
   uint8_t* out_scales;         // [rows][H/128] f32 (quant) or [rows][scale_row_bytes]
   float* out_w;                // 2D only
   int32_t* out_idx;            // 2D only
+  int32_t* err;
 };
 
 struct CombineParams {
@@ -91,6 +93,7 @@ struct CombineParams {
   const int32_t* row_map;      // standard MoE
   uint8_t* out;
   float* out_w;
+  int32_t* err;
 };
 
 struct ConvertParams {
@@ -164,6 +167,18 @@ cudaError_t launch_combine_2d(const CombineParams& p, int in_dtype, int out_dtyp
                               const LaunchCfg& lc, cudaStream_t st);
 cudaError_t launch_combine_std(const CombineParams& p, int in_dtype, int out_dtype,
                                const LaunchCfg& lc, cudaStream_t st);
+// Bulk-copy (TMA engine) combine; same results as the vector kernels. Needs
+// at most 8 rows per token (world_size <= 8, or top-k <= 8 for the packed layout).
+bool combine_bulk_supported(const CombineParams& p, bool std_layout);
+cudaError_t launch_combine_2d_bulk(const CombineParams& p, int in_dtype, int out_dtype,
+                                   const LaunchCfg& lc, cudaStream_t st);
+cudaError_t launch_combine_std_bulk(const CombineParams& p, int in_dtype, int out_dtype,
+                                    const LaunchCfg& lc, cudaStream_t st);
+// Copy-mode dispatch with bulk copies (TMA); same results as the vector
+// kernel. Needs source rows of at most 48 KB.
+bool dispatch_bulk_supported(const DispatchParams& p);
+cudaError_t launch_dispatch_bulk_copy(const DispatchParams& p, bool std_layout,
+                                      const LaunchCfg& lc, cudaStream_t st);
 cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
                                     const LaunchCfg& lc, cudaStream_t st);
 cudaError_t launch_convert_combine(const ConvertParams& p, int dtype, const LaunchCfg& lc,
@@ -223,6 +238,13 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
 
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Streaming store (evict-first): for outputs this kernel will not read again.
+__device__ __forceinline__ void st_v4_cs(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
 }

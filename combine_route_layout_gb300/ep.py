@@ -25,6 +25,7 @@ EP_ERR_STATE = -2
 EP_ERR_CAPACITY = -3
 EP_ERR_INVALID_INDEX = -4
 EP_ERR_CUDA = -5
+EP_ERR_TIMEOUT = -6
 EP_ERR_WORKSPACE = -7
 EP_ERR_UNSUPPORTED = -8
 
@@ -33,6 +34,9 @@ EP_DTYPE_FP32 = 1
 EP_DTYPE_FP8_E4M3 = 2
 EP_QUANT_NONE = 0
 EP_QUANT_FP8_E4M3_BLOCK128 = 1
+EP_COMBINE_AUTO = 0
+EP_COMBINE_VECTOR = 1
+EP_COMBINE_BULK = 2
 
 _TORCH_OF = {EP_DTYPE_BF16: torch.bfloat16, EP_DTYPE_FP32: torch.float32,
              EP_DTYPE_FP8_E4M3: torch.float8_e4m3fn}
@@ -50,7 +54,8 @@ class ep_config(ctypes.Structure):
         "world_size", "hidden_dim", "scale_dim", "scale_type_size", "max_token_type_size",
         "max_num_inp_token_per_rank", "num_experts_per_rank", "num_experts_per_token",
         "data_type", "quant_type", "combine_dtype", "combine_out_dtype", "weighted_combine",
-        "standard_moe", "max_packed_rows_per_rank", "block_num", "warp_num_per_block")]
+        "standard_moe", "max_packed_rows_per_rank", "block_num", "warp_num_per_block",
+        "combine_impl", "dispatch_impl", "use_external_inp_buf")]
 
 
 class ep_dispatch_out(ctypes.Structure):
@@ -91,6 +96,7 @@ def _load() -> ctypes.CDLL:
         "ep_sync": (S, [P, P]),
         "ep_last_error": (ctypes.c_char_p, []),
         "ep_routing_layout_noalloc": (S, [I, I, I, I, P, P, P, P, P, P, P]),
+        "ep_get_registered_combine_input_buffer": (S, [P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -148,6 +154,12 @@ def ep_combine(handle, expert_out, weights, indices, out, out_weights, call_rese
 def ep_get_dispatch_src_token_pos(handle) -> int:
     p = ctypes.c_void_p()
     _check(_lib.ep_get_dispatch_src_token_pos(handle, ctypes.byref(p)))
+    return p.value
+
+
+def ep_get_registered_combine_input_buffer(handle) -> int:
+    p = ctypes.c_void_p()
+    _check(_lib.ep_get_registered_combine_input_buffer(handle, ctypes.byref(p)))
     return p.value
 
 
@@ -221,6 +233,9 @@ class EpDispatchCombineConfig:
     weighted_combine: bool = False
     standard_moe: bool = False
     max_packed_rows_per_rank: int = 0
+    combine_impl: str = "auto"          # "auto" | "vector" | "bulk"
+    dispatch_impl: str = "auto"         # "auto" | "vector" | "bulk" (copy mode)
+    use_external_inp_buf: bool = True   # False: reserve a registered combine input buffer
 
     def to_c(self) -> ep_config:
         c = ep_config()
@@ -230,6 +245,9 @@ class EpDispatchCombineConfig:
                 v = _EP_OF[v]
             elif f.name == "quant_type":
                 v = {"none": EP_QUANT_NONE, "fp8_e4m3_block128": EP_QUANT_FP8_E4M3_BLOCK128}[v]
+            elif f.name in ("combine_impl", "dispatch_impl"):
+                v = {"auto": EP_COMBINE_AUTO, "vector": EP_COMBINE_VECTOR,
+                     "bulk": EP_COMBINE_BULK}[v]
             setattr(c, f.name, int(v))
         return c
 
@@ -320,16 +338,27 @@ class EpDispatchCombineOp:
         cfg = self.config
         R, T, H, k = (cfg.world_size, cfg.max_num_inp_token_per_rank, cfg.hidden_dim,
                       cfg.num_experts_per_token)
+        dev = self.workspace.device
         if out is None:
-            out = torch.empty((R, T, H), dtype=cfg.combine_out_dtype, device=input.device)
+            out = torch.empty((R, T, H), dtype=cfg.combine_out_dtype, device=dev)
         if out_weights is None and want_weights and weights is not None:
-            out_weights = torch.empty((R, T, k), dtype=torch.float32, device=input.device)
+            out_weights = torch.empty((R, T, k), dtype=torch.float32, device=dev)
         ep_combine(self._handle, _ptr(input), _ptr(weights), _ptr(indices), _ptr(out),
                    _ptr(out_weights), call_reset, _stream())
         return out, out_weights
 
     def reset(self):
         ep_reset(self._handle, _stream())
+
+    def get_registered_combine_input_buffer(self, dtype=None):
+        """Zero-copy combine input (User Guide, section 3): [R, cap, H] view of the
+        workspace buffer that combine(input=None) reads in place."""
+        cfg = self.config
+        dtype = cfg.combine_dtype if dtype is None else dtype
+        if dtype != cfg.combine_dtype:
+            raise EpError(EP_ERR_INVALID_ARG, "registered buffer holds combine_dtype")
+        p = ep_get_registered_combine_input_buffer(self._handle)
+        return self._view(p, dtype, (cfg.world_size, self.cap, cfg.hidden_dim))
 
     def get_dispatch_src_token_pos(self):
         p = ep_get_dispatch_src_token_pos(self._handle)

@@ -49,6 +49,7 @@ typedef enum {
     EP_ERR_CAPACITY = -3,       /* packed standard-MoE rows exceed the configured capacity */
     EP_ERR_INVALID_INDEX = -4,  /* expert id outside [-1, E) (or duplicated, standard MoE) */
     EP_ERR_CUDA = -5,           /* a CUDA runtime call failed; see ep_last_error() */
+    EP_ERR_TIMEOUT = -6,        /* a kernel's bounded wait gave up (reported by ep_sync) */
     EP_ERR_WORKSPACE = -7,      /* workspace NULL, misaligned or too small */
     EP_ERR_UNSUPPORTED = -8     /* valid request this build does not implement */
 } ep_status;
@@ -58,6 +59,24 @@ typedef enum {
     EP_DTYPE_FP32 = 1,
     EP_DTYPE_FP8_E4M3 = 2       /* OCP E4M3 (bias 7, max 448, NaN = S.1111.111) */
 } ep_dtype;
+
+typedef enum {
+    EP_COMBINE_AUTO = 0,        /* bulk for the 2D layout from 8192 source tokens on,
+                                   vector otherwise */
+    EP_COMBINE_VECTOR = 1,      /* 16-byte vector loads into registers */
+    EP_COMBINE_BULK = 2         /* bulk async copies (TMA) into a shared-memory ring; needs
+                                   <= 8 rows per token (world_size <= 8, or top-k <= 8
+                                   for the packed layout), else the vector kernel runs */
+} ep_combine_impl;
+
+typedef enum {
+    EP_DISPATCH_AUTO = 0,       /* bulk in copy mode from 8192 source tokens on, vector
+                                   otherwise */
+    EP_DISPATCH_VECTOR = 1,     /* 16-byte vector loads and stores */
+    EP_DISPATCH_BULK = 2        /* copy mode only: bulk async copies (TMA) through a
+                                   shared-memory ring, rows <= 48 KB; FP8 quantisation
+                                   always uses the vector kernel */
+} ep_dispatch_impl;
 
 typedef enum {
     EP_QUANT_NONE = 0,          /* dispatch moves the input bits unchanged */
@@ -91,6 +110,11 @@ typedef struct ep_config {
                                             R*Tmax*min(k,E_r) + 127*E_r */
     int32_t block_num;                   /* CTAs per launch; <= 0: one wave sized to the GPU */
     int32_t warp_num_per_block;          /* warps per CTA; <= 0: 8 */
+    int32_t combine_impl;                /* (+) ep_combine_impl */
+    int32_t dispatch_impl;               /* (+) ep_dispatch_impl */
+    int32_t use_external_inp_buf;        /* 1: combine reads the caller's expert_out (default);
+                                            0: also reserve a registered combine input buffer
+                                            (see ep_get_registered_combine_input_buffer) */
 } ep_config;
 
 typedef struct ep_handle ep_handle;
@@ -170,7 +194,8 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
  * sum the expert-output rows of its copies in ascending destination-rank
  * order in an f32 accumulator starting at +0, weighted by the rank's slot
  * weights when weighted_combine, and round once to combine_out_dtype.
- *   expert_out   device [R][cap][H] combine_dtype, rows in dispatch order
+ *   expert_out   device [R][cap][H] combine_dtype, rows in dispatch order; NULL
+ *                reads the registered combine input buffer (use_external_inp_buf = 0)
  *   weights      device [R][cap][k] f32 in receive layout (dispatch's weights
  *                output or the caller's), or NULL (then out_weights must be
  *                NULL and weighted_combine 0)
@@ -184,6 +209,16 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
 ep_status ep_combine(ep_handle* h, const void* expert_out, const float* weights,
                      const int32_t* indices, void* out, float* out_weights, int32_t call_reset,
                      void* stream);
+
+/*
+ * get_registered_combine_input_buffer() (User Guide, section 3; zero-copy
+ * mode, use_external_inp_buf = 0): device [R][cap][H] buffer of combine_dtype
+ * inside the workspace, valid for the handle's lifetime. Experts write their
+ * outputs there (row i of rank r for receive row i) and ep_combine with
+ * expert_out == NULL reads it in place. EP_ERR_STATE if the config did not
+ * reserve it.
+ */
+ep_status ep_get_registered_combine_input_buffer(ep_handle* h, void** d_buffer);
 
 /* get_dispatch_src_token_pos() (User Guide, section 3): device [R][cap]. */
 ep_status ep_get_dispatch_src_token_pos(ep_handle* h, const int32_t** d_src_token_pos);

@@ -47,7 +47,8 @@ def cfg(ep, **kw):
                 num_experts_per_token=8, data_type=ep.EP_DTYPE_BF16,
                 quant_type=ep.EP_QUANT_FP8_E4M3_BLOCK128, combine_dtype=ep.EP_DTYPE_BF16,
                 combine_out_dtype=ep.EP_DTYPE_BF16, weighted_combine=0, standard_moe=0,
-                max_packed_rows_per_rank=0, block_num=0, warp_num_per_block=0)
+                max_packed_rows_per_rank=0, block_num=0, warp_num_per_block=0, combine_impl=0,
+                dispatch_impl=0, use_external_inp_buf=1)
     base.update(kw)
     c = ep.ep_config()
     for k, v in base.items():
@@ -84,6 +85,19 @@ FAKE = 1 << 40   # an aligned address that is never dereferenced by these tests
 def small(ep, **kw):
     return cfg(ep, hidden_dim=256, max_num_inp_token_per_rank=16, num_experts_per_rank=4,
                num_experts_per_token=4, quant_type=0, **kw)
+
+
+def test_registered_buffer_is_reserved_in_the_workspace(ep):
+    a = ep.ep_workspace_size(small(ep))
+    b = ep.ep_workspace_size(small(ep, use_external_inp_buf=0))
+    assert b - a >= 8 * (8 * 16) * 256 * 2          # [R][cap][H] bf16
+    c = small(ep, use_external_inp_buf=0)
+    h = ep.ep_config_create(c, FAKE, b)
+    try:
+        p = ep.ep_get_registered_combine_input_buffer(h)
+        assert FAKE <= p < FAKE + b and p % 256 == 0
+    finally:
+        ep.ep_destroy(h)
 
 
 def test_workspace_checks(ep):
@@ -130,7 +144,10 @@ def test_state_machine_without_device(ep):
         with pytest.raises(ep.EpError) as ei:        # standard_moe = 0
             ep.ep_dispatch_standard_moe(h, FAKE, FAKE, None, FAKE, [1] * 8, None)
         assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        with pytest.raises(ep.EpError) as ei:        # no registered buffer reserved
+            ep.ep_get_registered_combine_input_buffer(h)
+        assert ei.value.status == ep.EP_ERR_STATE
         ep.ep_reset(h)
-        assert "standard_moe" in ep.ep_last_error()
+        assert "registered" in ep.ep_last_error()
     finally:
         ep.ep_destroy(h)

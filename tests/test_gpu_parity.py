@@ -420,8 +420,8 @@ def test_identity_invariant_bf16_dispatch():
 
 
 def test_repeated_rounds_random_shapes():
-    """Many dispatch -> combine -> reset rounds with changing token counts on
-    one handle (the tuning guide's repeated-round verification)."""
+    """500 dispatch -> combine -> reset rounds with changing token counts on
+    one handle (the tuning guide's 500-round verification)."""
     wl = WORKLOADS["tiny"].with_(tokens_per_rank=64, hidden=256)
     inp = Inputs(wl, 0)
     op = EpDispatchCombineOp(make_config(wl))
@@ -432,11 +432,11 @@ def test_repeated_rounds_random_shapes():
     for r in range(R):
         nD += (owners == r).any(-1).float()
     exp = inp.x.float() * nD[..., None]
-    for it in range(200):
+    for it in range(500):
         ntok = rng.integers(0, T + 1, size=R).astype(np.int32)
         d_x, d_w, _, _, recv = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, ntok)
         out, _ = op.combine(d_x, d_w, None, call_reset=True)
-        if it % 25 == 0:
+        if it % 50 == 0:
             op.sync()
             for s in range(R):
                 assert torch.equal(out[s, :ntok[s]], exp[s, :ntok[s]].to(out.dtype))
@@ -514,3 +514,183 @@ def test_fp8_quotients_on_e4m3_midpoints():
         assert np.array_equal(gsc[r, :n].view(np.uint32), sc_ref[r, :n].view(np.uint32))
         assert np.array_equal(gx[r, :n], x_ref[r, :n]), f"codes rank {r}"
     op.reset()
+
+
+# ------------------------------------------- bulk-copy (TMA) combine kernels
+
+@pytest.mark.parametrize("name,over,seed,ragged", [
+    ("tiny", {}, 0, False),
+    ("tiny", {}, 1, True),
+    ("ds_v3_latency", {}, 0, False),
+    ("ds_v3_throughput", dict(tokens_per_rank=300), 3, True),
+    ("mid_masked", dict(tokens_per_rank=600), 4, True),
+    ("mid_masked", dict(tokens_per_rank=130, hidden=1032, weighted=True), 7, True),
+    ("tiny", dict(hidden=264), 5, True),
+    ("tiny", dict(world_size=32, experts_per_rank=2, topk=8, tokens_per_rank=40), 5, True),
+])
+def test_bulk_combine_2d(name, over, seed, ragged):
+    run_2d(WORKLOADS[name].with_(**over), seed=seed, ragged=ragged,
+           cfg_over=dict(combine_impl="bulk"))
+
+
+@pytest.mark.parametrize("yd,od", [(torch.float32, torch.float32), (torch.float32, torch.bfloat16),
+                                   (torch.bfloat16, torch.float32)])
+def test_bulk_combine_dtypes(yd, od):
+    wl = WORKLOADS["mid_masked"].with_(tokens_per_rank=100, hidden=2056)
+    run_2d(wl, seed=6, ragged=True, y_dtype=yd, cfg_over=dict(combine_out_dtype=od,
+                                                              combine_impl="bulk"))
+
+
+@pytest.mark.parametrize("over", [dict(tokens_per_rank=300),
+                                  dict(router="uniform", mask_prob=0.2, tokens_per_rank=200),
+                                  dict(weighted=False, combine_out_dtype="bf16", hidden=1032),
+                                  dict(world_size=4, experts_per_rank=5, topk=3, hidden=384)])
+def test_bulk_combine_std(over):
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(hidden=1024).with_(**over)
+    run_std(wl, seed=2, ragged=True, cfg_over=dict(combine_impl="bulk"))
+
+
+@pytest.mark.slow
+def test_bulk_combine_full_size():
+    run_2d(WORKLOADS["ds_v3_throughput"], full=False, cfg_over=dict(combine_impl="bulk"))
+    run_std(WORKLOADS["skewed_zipf_std_moe"], full=False, cfg_over=dict(combine_impl="bulk"))
+
+
+# ------------------------------------------------------------- codec sweeps
+
+def test_gpu_e4m3_codes_for_every_bf16_value():
+    """Every finite bf16 value with |x| <= 448 passes through the FP8 dispatch
+    with a block scale of exactly 1 (each block holds 448), so the codes are
+    E4M3(x) and must equal the oracle's encoder."""
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (allb.astype(np.uint32) << 16).view(np.float32)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 448.0)
+    bits = allb[keep]
+    per_block = 127
+    nblk = -(-len(bits) // per_block)
+    H = 1024
+    tokens = -(-nblk // (H // 128))
+    R, T = 1, tokens
+    x = np.zeros((R, T, H), np.uint16)
+    flat = x.reshape(-1, 128)
+    flat[:, 127] = 0x43E0                        # bf16 448.0 in every block: scale 1
+    for b in range(nblk):
+        chunk = bits[b * per_block:(b + 1) * per_block]
+        flat[b, :len(chunk)] = chunk
+    wl = WORKLOADS["tiny"].with_(world_size=R, experts_per_rank=1, topk=1, tokens_per_rank=T,
+                                 hidden=H, dispatch_dtype="fp8", expert_output="random")
+    idx = np.zeros((R, T, 1), np.int32)
+    w = np.ones((R, T, 1), np.float32)
+    op = EpDispatchCombineOp(make_config(wl))
+    xd = torch.from_numpy(x.view(np.int16)).to(DEV).view(torch.bfloat16)
+    d_x, _, d_sc, _, recv = op.dispatch(xd, torch.from_numpy(w).to(DEV), None,
+                                         torch.from_numpy(idx).to(DEV), [T])
+    op.sync()
+    q_ref, sc_ref = oracle.quant_tokens(x)
+    assert np.all(sc_ref == 1.0)
+    assert np.array_equal(host(d_x)[0, :T], q_ref[0])
+    op.reset()
+
+
+def test_gpu_bf16_rounding_sweep():
+    """A million random f32 bit patterns through an f32-in / bf16-out combine
+    with one copy per token: the output is the GPU's bf16 rounding of +0 + y,
+    compared with the oracle's."""
+    rng = np.random.default_rng(3)
+    H, T = 1024, 1024
+    u = rng.integers(0, 2**32, size=(T, H), dtype=np.uint64).astype(np.uint32)
+    u[:, :64] = (rng.integers(0, 2**16, size=(T, 64), dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    y = u.view(np.float32)
+    y[~np.isfinite(y)] = 1.0
+    wl = WORKLOADS["tiny"].with_(world_size=1, experts_per_rank=1, topk=1, tokens_per_rank=T,
+                                 hidden=H, combine_out_dtype="bf16")
+    idx = np.zeros((1, T, 1), np.int32)
+    w = np.ones((1, T, 1), np.float32)
+    op = EpDispatchCombineOp(make_config(wl, combine_dtype=torch.float32))
+    x = torch.zeros((1, T, H), dtype=torch.bfloat16, device=DEV)
+    d = op.dispatch(x, torch.from_numpy(w).to(DEV), None, torch.from_numpy(idx).to(DEV), [T])
+    yd = torch.from_numpy(y.reshape(1, T, H).copy()).to(DEV)
+    out, _ = op.combine(yd, d[1], None, call_reset=True)
+    op.sync()
+    recv, src_pos, slot = oracle.route(idx, np.array([T], np.int32), 1)
+    ref, _ = oracle.combine(y.reshape(1, T, H), idx, np.array([T], np.int32), slot, 1,
+                            out_dtype="bf16")
+    assert np.array_equal(host(out), ref)
+
+
+def test_registered_combine_input_buffer_zero_copy():
+    """Zero-copy mode (use_external_inp_buf = 0): experts write into the
+    library's registered buffer and combine reads it in place."""
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=100)
+    R, T = wl.world_size, wl.tokens_per_rank
+    inp = Inputs(wl, 1, ragged=True)
+    op = EpDispatchCombineOp(make_config(wl, use_external_inp_buf=False))
+    d_x, d_w, _, _, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    buf = op.get_registered_combine_input_buffer()
+    y = make_expert_outputs(wl, R * T, 1, device=DEV)
+    buf.copy_(y)
+    out, outw = op.combine(None, d_w, None, call_reset=True)
+    op.sync()
+    recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, wl.experts_per_rank)
+    w_ref = oracle.place_rows(inp.w, inp.ntok, slot)
+    ref, ref_w = oracle.combine(host(y), inp.idx, inp.ntok, slot, wl.experts_per_rank,
+                                w_recv=w_ref, out_dtype="bf16")
+    go, gw = host(out), host(outw)
+    for s in range(R):
+        n = inp.ntok[s]
+        assert np.array_equal(go[s, :n], ref[s, :n])
+        assert np.array_equal(gw[s, :n].view(np.uint32), ref_w[s, :n].view(np.uint32))
+
+
+# ------------------------------------------ bulk-copy (TMA) dispatch kernels
+
+@pytest.mark.parametrize("name,over,seed,ragged", [
+    ("tiny", {}, 0, False),
+    ("tiny", {}, 1, True),
+    ("mid_masked", dict(tokens_per_rank=600), 4, True),
+    ("mid_masked", dict(tokens_per_rank=300, hidden=1032, mask_prob=0.9), 2, True),
+    ("tiny", dict(world_size=32, experts_per_rank=2, topk=8, tokens_per_rank=40), 5, True),
+    ("tiny", dict(world_size=1, experts_per_rank=8, topk=4), 5, True),
+])
+def test_bulk_dispatch_2d(name, over, seed, ragged):
+    run_2d(WORKLOADS[name].with_(**over), seed=seed, ragged=ragged,
+           cfg_over=dict(dispatch_impl="bulk", combine_impl="bulk"))
+
+
+@pytest.mark.parametrize("over", [dict(tokens_per_rank=300),
+                                  dict(router="uniform", mask_prob=0.2, tokens_per_rank=200),
+                                  dict(world_size=4, experts_per_rank=5, topk=3, hidden=384)])
+def test_bulk_dispatch_std(over):
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(hidden=1024).with_(**over)
+    run_std(wl, seed=2, ragged=True, cfg_over=dict(dispatch_impl="bulk"))
+
+
+def test_bulk_dispatch_fp8_passthrough_with_scales():
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=70, hidden=1024)
+    R, T, H = wl.world_size, wl.tokens_per_rank, wl.hidden
+    inp = Inputs(wl, 8, ragged=True)
+    codes = torch.randint(0, 126, (R, T, H), dtype=torch.uint8, device=DEV)
+    scales = torch.rand((R, T, H // 128), device=DEV, dtype=torch.float32)
+    cfg = make_config(wl, data_type=torch.float8_e4m3fn, quant_type="none", scale_dim=H // 128,
+                      scale_type_size=4, dispatch_impl="bulk")
+    op = EpDispatchCombineOp(cfg)
+    d_x, d_w, d_sc, d_idx, recv_d = op.dispatch(codes.view(torch.float8_e4m3fn), inp.w_d, scales,
+                                                inp.idx_d, inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    x_ref = oracle.place_rows(host(codes), inp.ntok, slot)
+    sc_ref = oracle.place_rows(host(scales), inp.ntok, slot)
+    w_ref = oracle.place_rows(inp.w, inp.ntok, slot)
+    gx, gs, gw = host(d_x), host(d_sc).view(np.float32), host(d_w)
+    for r in range(R):
+        n = recv[r]
+        assert np.array_equal(gx[r, :n], x_ref[r, :n])
+        assert np.array_equal(gs[r, :n].reshape(n, -1).view(np.uint32), sc_ref[r, :n].view(np.uint32))
+        assert np.array_equal(gw[r, :n].view(np.uint32), w_ref[r, :n].view(np.uint32))
+    op.reset()
+
+
+@pytest.mark.slow
+def test_bulk_dispatch_full_size():
+    run_2d(WORKLOADS["mid_masked"], full=False, cfg_over=dict(dispatch_impl="bulk"))
+    run_std(WORKLOADS["skewed_zipf_std_moe"], full=False, cfg_over=dict(dispatch_impl="bulk"))
