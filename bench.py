@@ -50,18 +50,16 @@ def algorithmic_bytes(wl, C: int, P: int, Ttot: int) -> dict:
     weights. Standard MoE moves one row per valid (token, slot).
     """
     H, k = wl.hidden, wl.topk
-    nb = H // 128
-    fp8 = wl.dispatch_dtype == "fp8"
-    b = 1 if fp8 else 2
+    row = {"fp8": H + 4 * (H // 128), "fp4": H // 2 + 4 * (H // 32)}.get(wl.dispatch_dtype, 2 * H)
     bo = 4 if wl.combine_out_dtype == "fp32" else 2
     if not wl.standard_moe:
         d_read = Ttot * (2 * H + 8 * k)
-        d_write = C * (H * b + (4 * nb if fp8 else 0) + 8 * k + 4)
+        d_write = C * (row + 8 * k + 4)
         c_read = C * (2 * H + 4 * k + 4)
         c_write = Ttot * (H * bo + 4 * k)
     else:
         d_read = Ttot * (2 * H + 8 * k)
-        d_write = P * (H * b + (4 * nb if fp8 else 0) + 4)
+        d_write = P * (row + 4)
         c_read = P * (2 * H + 4) + Ttot * 8 * k
         c_write = Ttot * bo * H
     return {"dispatch": d_read + d_write, "combine": c_read + c_write,
@@ -150,6 +148,10 @@ class ClockSampler:
 
 COMBINE_IMPL = "auto"
 DISPATCH_IMPL = "auto"
+E2E_STREAMS = 2
+
+
+LAUNCH = {"block_num": -1, "warp_num_per_block": 8}
 
 
 def make_op(wl, device):
@@ -159,11 +161,13 @@ def make_op(wl, device):
         scale_type_size=4, max_token_type_size=4,
         max_num_inp_token_per_rank=wl.tokens_per_rank,
         num_experts_per_rank=wl.experts_per_rank, num_experts_per_token=wl.topk,
-        quant_type="fp8_e4m3_block128" if wl.dispatch_dtype == "fp8" else "none",
+        quant_type={"fp8": "fp8_e4m3_block128", "fp4": "fp4_e2m1_block32"}.get(wl.dispatch_dtype,
+                                                                            "none"),
         combine_dtype=torch.bfloat16,
         combine_out_dtype=torch.float32 if wl.combine_out_dtype == "fp32" else torch.bfloat16,
         weighted_combine=wl.weighted, standard_moe=wl.standard_moe, combine_impl=COMBINE_IMPL,
-        dispatch_impl=DISPATCH_IMPL)
+        dispatch_impl=DISPATCH_IMPL, block_num=LAUNCH["block_num"],
+        warp_num_per_block=LAUNCH["warp_num_per_block"])
     return EpDispatchCombineOp(cfg, device)
 
 
@@ -307,13 +311,22 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
     h2d = xh.numel() * xh.element_size() + wh.numel() * 4 + ih.numel() * 4 + ybytes
     d2h = oh.numel() * oh.element_size()
 
+    # The expert-output rows do not depend on dispatch: they travel on side
+    # streams (other copy engines) while the tokens are copied and dispatched.
+    side = [torch.cuda.Stream() for _ in range(E2E_STREAMS)]
+
     def one():
+        for sd in side:
+            sd.wait_stream(st)                  # previous combine has read y
+        for j, (hsrc, ddst) in enumerate(ycopy):
+            with torch.cuda.stream(side[j % len(side)]):
+                ddst.copy_(hsrc, non_blocking=True)
         xd.copy_(xh, non_blocking=True)
         wd.copy_(wh, non_blocking=True)
         idd.copy_(ih, non_blocking=True)
-        for hsrc, ddst in ycopy:
-            ddst.copy_(hsrc, non_blocking=True)
         d = step.dispatch(xd, wd, idd)
+        for sd in side:
+            st.wait_stream(sd)
         step.combine(d, w=wd)
         oh.copy_(step.out, non_blocking=True)
 
@@ -350,6 +363,7 @@ def cpu_oracle_step(wl, tokens_per_rank: int, seed: int = 0, y=None):
             y = make_expert_outputs(sw, pcap, seed).view(torch.int16).numpy().view(np.uint16)
         t = time.perf_counter()
         res = oracle.std_dispatch(x, idx, ntok, Er, pcap, quant_fp8=sw.dispatch_dtype == "fp8")
+        # (the packed-layout oracle quantises FP8 only; FP4 workloads use the 2D layout)
         oracle.std_combine(y, idx, ntok, res["row_map"], Er, w=w, weighted=sw.weighted,
                            out_dtype=od)
         dt = time.perf_counter() - t
@@ -359,7 +373,8 @@ def cpu_oracle_step(wl, tokens_per_rank: int, seed: int = 0, y=None):
         if y is None:
             y = make_expert_outputs(sw, R * T, seed).view(torch.int16).numpy().view(np.uint16)
         t = time.perf_counter()
-        d = oracle.dispatch(x, w, idx, ntok, Er, quant_fp8=sw.dispatch_dtype == "fp8")
+        d = oracle.dispatch(x, w, idx, ntok, Er, quant_fp8=sw.dispatch_dtype == "fp8",
+                            quant_fp4=sw.dispatch_dtype == "fp4")
         oracle.combine(y, idx, ntok, d["slot"], Er, w_recv=d["w"], weighted=sw.weighted,
                        out_dtype=od)
         dt = time.perf_counter() - t
@@ -381,6 +396,33 @@ def cpu_baseline(wl, sample_tokens: int, reps: int):
 
 
 # ----------------------------------------------------------- main
+
+def sweep(wl, dev, K: int, W: int):
+    """Launch-configuration sweep (the local counterpart of a launch tuner):
+    dispatch and combine times over block_num x warp_num_per_block for the
+    vector kernels, plus the library's automatic choice. One JSON line."""
+    global COMBINE_IMPL, DISPATCH_IMPL
+    results = []
+    grids = [-1, 152, 304, 456, 608, 912, 1216]
+    warps = [4, 8]
+    for impl in ("vector", "auto"):
+        COMBINE_IMPL = DISPATCH_IMPL = impl
+        for bn in (grids if impl == "vector" else [-1]):
+            for wp in (warps if impl == "vector" else [8]):
+                LAUNCH["block_num"], LAUNCH["warp_num_per_block"] = bn, wp
+                step = Step(wl, dev)
+                _, disp, comb = time_steps(step, K, W, None, lambda: None)
+                results.append({"impl": impl, "block_num": bn, "warp_num_per_block": wp,
+                                "dispatch_us": round(statistics.median(disp) * 1e3, 2),
+                                "combine_us": round(statistics.median(comb) * 1e3, 2)})
+                del step
+                torch.cuda.empty_cache()
+    LAUNCH["block_num"], LAUNCH["warp_num_per_block"] = -1, 8
+    best_d = min(results, key=lambda r: r["dispatch_us"])
+    best_c = min(results, key=lambda r: r["combine_us"])
+    return {"sweep": wl.name, "results": results, "best_dispatch": best_d,
+            "best_combine": best_c}
+
 
 def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
@@ -455,23 +497,28 @@ def main():
     ap.add_argument("--latency-workload", default="ds_v3_latency")
     ap.add_argument("--combine-impl", default="auto", choices=["auto", "vector", "bulk"])
     ap.add_argument("--dispatch-impl", default="auto", choices=["auto", "vector", "bulk"])
+    ap.add_argument("--sweep", action="store_true",
+                    help="time dispatch/combine over launch configurations instead")
+    ap.add_argument("--e2e-streams", type=int, default=2,
+                    help="side streams carrying the expert-output H2D copies in the e2e leg")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override the workload's tokens per rank (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=512,
+    ap.add_argument("--cpu-tokens", type=int, default=1024,
                     help="tokens/rank of the CPU-oracle baseline sample")
-    ap.add_argument("--cpu-reps", type=int, default=2)
+    ap.add_argument("--cpu-reps", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="tokens/rank per step of the reference (oracle) arm")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    global COMBINE_IMPL, DISPATCH_IMPL
+    global COMBINE_IMPL, DISPATCH_IMPL, E2E_STREAMS
     COMBINE_IMPL = args.combine_impl
     DISPATCH_IMPL = args.dispatch_impl
+    E2E_STREAMS = max(1, args.e2e_streams)
     rank, world, local = dist_setup(args.gpus)
     wl = WORKLOADS[args.workload]
     if args.tokens_per_rank > 0:
@@ -484,6 +531,10 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.sweep:
+        if rank == 0:
+            print(json.dumps(sweep(wl, dev, args.steps, args.warmup)), flush=True)
+        return
     barrier = barrier_fn(world)
     step = Step(wl, dev)
     peak, peak_src = hbm_peak()
@@ -510,7 +561,7 @@ def main():
         and wl.world_size <= 8 and not wl.standard_moe
     dom_kernel = {"combine": "combine_bulk_kernel" if bulk else
                   ("combine_std_kernel" if wl.standard_moe else "combine_2d_kernel"),
-                  "dispatch": "dispatch_quant_kernel" if wl.dispatch_dtype == "fp8"
+                  "dispatch": "dispatch_quant_kernel" if wl.dispatch_dtype in ("fp8", "fp4")
                   else "dispatch_copy_kernel"}[dom]
     ach = c_gbs if dom == "combine" else d_gbs
     tr = profiled_traffic(dom_key)

@@ -9,7 +9,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
+#include <tuple>
 
 #include "ep_kernels.cuh"
 
@@ -42,6 +45,7 @@ int dtype_size(int dt) {
     case EP_DTYPE_BF16: return 2;
     case EP_DTYPE_FP32: return 4;
     case EP_DTYPE_FP8_E4M3: return 1;
+    case EP_DTYPE_FP4_E2M1X2: return 1;   // two elements per byte (row bytes = H/2)
     default: return 0;
   }
 }
@@ -156,9 +160,11 @@ ep_status make_geometry(const ep_config* cfg, Geometry* g) {
     return fail(EP_ERR_INVALID_ARG, "world_size^2 * max tokens exceeds the int32 src_token_pos range");
   const int in_sz = dtype_size(cfg->data_type);
   if (in_sz == 0) return fail(EP_ERR_INVALID_ARG, "unknown data_type %d", cfg->data_type);
-  if (cfg->quant_type != EP_QUANT_NONE && cfg->quant_type != EP_QUANT_FP8_E4M3_BLOCK128)
+  if (cfg->quant_type != EP_QUANT_NONE && cfg->quant_type != EP_QUANT_FP8_E4M3_BLOCK128 &&
+      cfg->quant_type != EP_QUANT_FP4_E2M1_BLOCK32)
     return fail(EP_ERR_INVALID_ARG, "unknown quant_type %d", cfg->quant_type);
-  const bool quant = cfg->quant_type == EP_QUANT_FP8_E4M3_BLOCK128;
+  const bool quant = cfg->quant_type != EP_QUANT_NONE;
+  const int qblock = cfg->quant_type == EP_QUANT_FP4_E2M1_BLOCK32 ? 32 : EP_QUANT_BLOCK;
   if (cfg->combine_dtype != EP_DTYPE_BF16 && cfg->combine_dtype != EP_DTYPE_FP32)
     return fail(EP_ERR_INVALID_ARG, "combine_dtype must be BF16 or FP32");
   if (cfg->combine_out_dtype != EP_DTYPE_BF16 && cfg->combine_out_dtype != EP_DTYPE_FP32)
@@ -184,18 +190,21 @@ ep_status make_geometry(const ep_config* cfg, Geometry* g) {
   x.std_moe = cfg->standard_moe != 0;
   x.registered_in = cfg->use_external_inp_buf == 0;
   x.combine_in_row_bytes = (int64_t)H * dtype_size(cfg->combine_dtype);
-  x.in_row_bytes = (int64_t)H * in_sz;
+  x.in_row_bytes = cfg->data_type == EP_DTYPE_FP4_E2M1X2 ? (int64_t)H / 2 : (int64_t)H * in_sz;
+  if (cfg->data_type == EP_DTYPE_FP4_E2M1X2 && H % 32 != 0)
+    return fail(EP_ERR_INVALID_ARG, "packed FP4 input needs hidden_dim %% 32 == 0");
   if (x.in_row_bytes % 16 != 0)
     return fail(EP_ERR_INVALID_ARG, "hidden_dim * element size must be a multiple of 16 bytes");
   if (quant) {
     if (cfg->data_type != EP_DTYPE_BF16)
-      return fail(EP_ERR_INVALID_ARG, "FP8 block quantisation needs BF16 input");
-    if (H % EP_QUANT_BLOCK != 0)
-      return fail(EP_ERR_INVALID_ARG, "FP8 block quantisation needs hidden_dim %% 128 == 0");
-    if (cfg->scale_dim != 0 && !(cfg->scale_dim == H / EP_QUANT_BLOCK && cfg->scale_type_size == 4))
-      return fail(EP_ERR_INVALID_ARG, "with FP8 block quantisation scale_dim must be 0 or hidden_dim/128 (4-byte)");
-    x.out_row_bytes = H;
-    x.scale_row_bytes = H / EP_QUANT_BLOCK * 4;
+      return fail(EP_ERR_INVALID_ARG, "block quantisation needs BF16 input");
+    if (H % qblock != 0)
+      return fail(EP_ERR_INVALID_ARG, "block quantisation needs hidden_dim %% %d == 0", qblock);
+    if (cfg->scale_dim != 0 && !(cfg->scale_dim == H / qblock && cfg->scale_type_size == 4))
+      return fail(EP_ERR_INVALID_ARG,
+                  "with block quantisation scale_dim must be 0 or hidden_dim/%d (4-byte)", qblock);
+    x.out_row_bytes = cfg->quant_type == EP_QUANT_FP4_E2M1_BLOCK32 ? H / 2 : H;
+    x.scale_row_bytes = H / qblock * 4;
     x.in_scale_row_bytes = 0;
   } else {
     x.out_row_bytes = x.in_row_bytes;
@@ -226,6 +235,28 @@ ep_status device_sm_count(int* out) {
 }
 
 }  // namespace
+
+int ep::ctas_per_sm(const void* kernel, int block, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, size_t, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const auto key = std::make_tuple(kernel, block, smem, dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  if (smem > 48 * 1024)
+    (void)cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess ||
+      n < 1)
+    n = 1;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
+}
 
 ep_status ep::record_error(ep_status st, const char* msg) {
   g_last_error = msg;
@@ -431,8 +462,9 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
   dp.out_w = h->w.recv_w;
   dp.out_idx = h->w.recv_idx;
   dp.err = h->w.err;
-  e = use_bulk_dispatch(h, dp) ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h), st)
-                               : ep::launch_dispatch_2d(dp, h->g.quant, launch_cfg(h), st);
+  e = use_bulk_dispatch(h, dp)
+          ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h), st)
+          : ep::launch_dispatch_2d(dp, h->g.quant ? h->cfg.quant_type : 0, launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
 
   h->state = kDispatched;
@@ -559,8 +591,9 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
   dp.out_x = h->w.packed_x;
   dp.out_scales = h->w.packed_scales;
   dp.err = h->w.err;
-  e = use_bulk_dispatch(h, dp) ? ep::launch_dispatch_bulk_copy(dp, true, launch_cfg(h), st)
-                               : ep::launch_dispatch_std(dp, h->g.quant, launch_cfg(h), st);
+  e = use_bulk_dispatch(h, dp)
+          ? ep::launch_dispatch_bulk_copy(dp, true, launch_cfg(h), st)
+          : ep::launch_dispatch_std(dp, h->g.quant ? h->cfg.quant_type : 0, launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "standard-MoE dispatch launch");
 
   h->state = kDispatched;

@@ -197,14 +197,23 @@ __global__ void __launch_bounds__(256) combine_std_kernel(CombineParams p) {
   const int64_t in_row = (int64_t)p.H * dt_size(IN);
   const int64_t out_row = (int64_t)p.H * dt_size(OUT);
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
-       u += nwarps) {
+  // packed row of slot `lane` of unit u's token (-1: none)
+  auto row_of = [&](int64_t u) -> int {
+    if (u >= p.total_units || lane >= p.k) return -1;
+    const int64_t g = u / p.segs_per_token;
+    const int s = (int)(g / p.Tmax), t = (int)(g - (int64_t)s * p.Tmax);
+    return t < p.ntok[s] ? __ldg(p.row_map + g * p.k + lane) : -1;
+  };
+  int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int row_next = row_of(u);
+  for (; u < p.total_units; u += nwarps) {
+    const int row = row_next;
+    row_next = row_of(u + nwarps);  // prefetch: overlaps this unit's row loads
     const int64_t g = u / p.segs_per_token;
     const int seg = (int)(u - g * p.segs_per_token);
     const int s = (int)(g / p.Tmax), t = (int)(g - (int64_t)s * p.Tmax);
     if (t >= p.ntok[s]) continue;
 
-    const int row = lane < p.k ? __ldg(p.row_map + g * p.k + lane) : -1;
     const bool valid = row >= 0;
     const int key = valid ? (int)(row / p.cap) * 32 + lane : 0x7FFFFFFF;
     const float wj = (valid && p.weighted) ? __ldg(p.w + g * p.k + lane) : 0.0f;

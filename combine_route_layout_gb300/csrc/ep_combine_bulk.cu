@@ -245,12 +245,7 @@ cudaError_t launch_bulk(const CombineParams& p0, int in_dtype, int out_dtype, co
          : (ob ? combine_bulk_kernel<STD, EP_DTYPE_FP32, EP_DTYPE_BF16>
                : combine_bulk_kernel<STD, EP_DTYPE_FP32, EP_DTYPE_FP32>);
   const size_t smem = ib ? sizeof(Ring<EP_DTYPE_BF16>) : sizeof(Ring<EP_DTYPE_FP32>);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  const int per_sm = ctas_per_sm(k, kThreads, smem);  // also raises the smem limit
   int64_t grid = lc.grid_hint > 0 ? lc.grid_hint : (int64_t)lc.sm_count * per_sm;
   const int64_t ntokens = (int64_t)p.R * p.Tmax;
   if (grid > ntokens) grid = ntokens;

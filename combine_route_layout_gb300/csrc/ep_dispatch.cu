@@ -158,14 +158,18 @@ __global__ void __launch_bounds__(256, 4) dispatch_copy_kernel(DispatchParams p)
 // 512-element step, so 8 lanes cover one 128-element block; the block's amax
 // is reduced with three xor-shuffles inside that 8-lane group.
 
-__device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q, float& scale) {
-  float f[16];
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float f[16]) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     f[2 * i] = bf16_lo(w[i]);
     f[2 * i + 1] = bf16_hi(w[i]);
   }
+}
+
+__device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q, float& scale) {
+  float f[16];
+  unpack16(a, b, f);
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -188,10 +192,29 @@ __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q
   q.w = c[6] | (c[7] << 16);
 }
 
-template <bool STD>
+// FP4: the same 16 elements per lane, now half of a 32-element block; the
+// block's amax is reduced over the lane pair, scale = amax / 6.
+__device__ __forceinline__ void quant16_fp4(const uint4& a, const uint4& b, uint2& q,
+                                            float& scale) {
+  float f[16];
+  unpack16(a, b, f);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  scale = __fdiv_rn(amax, 6.0f);
+  if (amax != 0.f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], scale);
+  }
+  q.x = cvt_e2m1x8(f);
+  q.y = cvt_e2m1x8(f + 8);
+}
+
+template <bool STD, bool FP4>
 __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p) {
   const int lane = threadIdx.x & 31;
-  const int nb = p.H / 128;
+  const int nb = p.H / (FP4 ? 32 : 128);
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   bool waited = false;
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
@@ -215,9 +238,13 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
       }
     }
     uint4 q[kQuantUnroll];
+    uint2 q4[kQuantUnroll];
     float sc[kQuantUnroll];
 #pragma unroll
-    for (int i = 0; i < kQuantUnroll; ++i) quant16(a[i], b[i], q[i], sc[i]);
+    for (int i = 0; i < kQuantUnroll; ++i) {
+      if (FP4) quant16_fp4(a[i], b[i], q4[i], sc[i]);
+      else quant16(a[i], b[i], q[i], sc[i]);
+    }
     if (!waited) {  // the routing layout is complete and visible past this point
       pdl_wait();
       waited = true;
@@ -231,8 +258,13 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
       for (int i = 0; i < kQuantUnroll; ++i) {
         const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
         if (e0 < p.H) {
-          st_v4(dst + e0, q[i]);
-          if ((lane & 7) == 0) dsc[e0 / 128] = sc[i];
+          if (FP4) {
+            st_v2(dst + e0 / 2, q4[i]);
+            if ((lane & 1) == 0) dsc[e0 / 32] = sc[i];
+          } else {
+            st_v4(dst + e0, q[i]);
+            if ((lane & 7) == 0) dsc[e0 / 128] = sc[i];
+          }
         }
       }
     };
@@ -258,21 +290,23 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
 }
 
 template <bool STD>
-cudaError_t launch_dispatch(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+cudaError_t launch_dispatch(const DispatchParams& p, int quant, const LaunchCfg& lc,
                             cudaStream_t st) {
   if (p.total_units == 0) return cudaSuccess;
-  auto k = quant ? dispatch_quant_kernel<STD> : dispatch_copy_kernel<STD>;
+  auto k = quant == EP_QUANT_FP8_E4M3_BLOCK128  ? dispatch_quant_kernel<STD, false>
+           : quant == EP_QUANT_FP4_E2M1_BLOCK32 ? dispatch_quant_kernel<STD, true>
+                                                : dispatch_copy_kernel<STD>;
   return launch_pdl(k, auto_grid(k, lc, p.total_units), lc.block, 0, st, p);
 }
 
 }  // namespace
 
-cudaError_t launch_dispatch_2d(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+cudaError_t launch_dispatch_2d(const DispatchParams& p, int quant, const LaunchCfg& lc,
                                cudaStream_t st) {
   return launch_dispatch<false>(p, quant, lc, st);
 }
 
-cudaError_t launch_dispatch_std(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+cudaError_t launch_dispatch_std(const DispatchParams& p, int quant, const LaunchCfg& lc,
                                 cudaStream_t st) {
   return launch_dispatch<true>(p, quant, lc, st);
 }

@@ -154,12 +154,7 @@ cudaError_t launch_dispatch_bulk_copy(const DispatchParams& p, bool std_layout,
   if (ntokens == 0) return cudaSuccess;
   auto k = std_layout ? dispatch_bulk_copy_kernel<true> : dispatch_bulk_copy_kernel<false>;
   const size_t smem = 128 + (size_t)kStages * p.in_row_bytes;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 32, smem) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  const int per_sm = ctas_per_sm(k, 32, smem);  // also raises the smem limit
   int64_t grid = lc.grid_hint > 0 ? lc.grid_hint : (int64_t)lc.sm_count * per_sm;
   if (grid > ntokens) grid = ntokens;
   return launch_pdl(k, (int)grid, 32, smem, st, p);

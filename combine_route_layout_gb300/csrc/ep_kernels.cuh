@@ -138,6 +138,17 @@ struct LaunchCfg {
   int sm_count;
 };
 
+// Resident CTAs per SM for (kernel, block, dynamic smem) on the current
+// device; raises the kernel's dynamic shared-memory limit first when smem
+// exceeds the default. Cached after the first query, so a launch costs no
+// occupancy calculation.
+int ctas_per_sm(const void* kernel, int block, size_t smem);
+
+template <typename Kernel>
+inline int ctas_per_sm(Kernel kernel, int block, size_t smem = 0) {
+  return ctas_per_sm(reinterpret_cast<const void*>(kernel), block, smem);
+}
+
 // CTAs for a grid-stride kernel over `units` warp-sized work units: the
 // caller's request, else as many CTAs as fit on the GPU at once, never more
 // than the units need.
@@ -146,22 +157,17 @@ inline int auto_grid(Kernel kernel, const LaunchCfg& lc, int64_t units, size_t s
   const int64_t warps = lc.block / 32;
   const int64_t need = (units + warps - 1) / warps;
   int64_t grid = lc.grid_hint;
-  if (grid <= 0) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, lc.block, smem) !=
-            cudaSuccess || per_sm < 1)
-      per_sm = 1;
-    grid = (int64_t)lc.sm_count * per_sm;
-  }
+  if (grid <= 0) grid = (int64_t)lc.sm_count * ctas_per_sm(kernel, lc.block, smem);
   if (grid > need) grid = need;
   return grid < 1 ? 1 : (int)grid;
 }
 
 cudaError_t launch_layout_2d(const LayoutParams& p, cudaStream_t st);
 cudaError_t launch_layout_std(const LayoutParams& p, cudaStream_t st);
-cudaError_t launch_dispatch_2d(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+// quant: 0 = copy, EP_QUANT_FP8_E4M3_BLOCK128 or EP_QUANT_FP4_E2M1_BLOCK32.
+cudaError_t launch_dispatch_2d(const DispatchParams& p, int quant, const LaunchCfg& lc,
                                cudaStream_t st);
-cudaError_t launch_dispatch_std(const DispatchParams& p, bool quant, const LaunchCfg& lc,
+cudaError_t launch_dispatch_std(const DispatchParams& p, int quant, const LaunchCfg& lc,
                                 cudaStream_t st);
 cudaError_t launch_combine_2d(const CombineParams& p, int in_dtype, int out_dtype,
                               const LaunchCfg& lc, cudaStream_t st);
@@ -255,6 +261,25 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Eight f32 -> eight OCP E2M1 codes, round to nearest even, saturating to
+// +-6; byte k holds elements 2k (low nibble) and 2k+1 (high nibble).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float f[8]) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+  return r;
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 // Two f32 -> two bf16 (round to nearest even); lo in bits 0..15.

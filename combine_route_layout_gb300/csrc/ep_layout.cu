@@ -225,11 +225,7 @@ cudaError_t launch_layout_2d(const LayoutParams& p, cudaStream_t st) {
 cudaError_t launch_layout_std(const LayoutParams& p, cudaStream_t st) {
   if (p.nchunks == 0) return cudaSuccess;
   const size_t smem = (size_t)kWarps * p.E * (sizeof(uint32_t) + 1);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(layout_std_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  if (smem > 48 * 1024) (void)ctas_per_sm(layout_std_kernel, kLayoutThreads, smem);
   layout_std_kernel<<<p.nchunks, kLayoutThreads, smem, st>>>(p);
   return cudaGetLastError();
 }

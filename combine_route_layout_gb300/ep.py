@@ -32,15 +32,22 @@ EP_ERR_UNSUPPORTED = -8
 EP_DTYPE_BF16 = 0
 EP_DTYPE_FP32 = 1
 EP_DTYPE_FP8_E4M3 = 2
+EP_DTYPE_FP4_E2M1X2 = 3
 EP_QUANT_NONE = 0
 EP_QUANT_FP8_E4M3_BLOCK128 = 1
+EP_QUANT_FP4_E2M1_BLOCK32 = 2
 EP_COMBINE_AUTO = 0
 EP_COMBINE_VECTOR = 1
 EP_COMBINE_BULK = 2
 
+_FP4X2 = getattr(torch, "float4_e2m1fn_x2", None)   # packed pairs of E2M1 codes
 _TORCH_OF = {EP_DTYPE_BF16: torch.bfloat16, EP_DTYPE_FP32: torch.float32,
              EP_DTYPE_FP8_E4M3: torch.float8_e4m3fn}
+if _FP4X2 is not None:
+    _TORCH_OF[EP_DTYPE_FP4_E2M1X2] = _FP4X2
 _EP_OF = {v: k for k, v in _TORCH_OF.items()}
+_QUANT_OF = {"none": EP_QUANT_NONE, "fp8_e4m3_block128": EP_QUANT_FP8_E4M3_BLOCK128,
+             "fp4_e2m1_block32": EP_QUANT_FP4_E2M1_BLOCK32}
 
 
 class EpError(RuntimeError):
@@ -227,7 +234,7 @@ class EpDispatchCombineConfig:
     num_experts_per_token: int
     warp_num_per_block: int = 8
     block_num: int = -1
-    quant_type: str = "none"            # "none" | "fp8_e4m3_block128"
+    quant_type: str = "none"            # "none" | "fp8_e4m3_block128" | "fp4_e2m1_block32"
     combine_dtype: torch.dtype = torch.bfloat16
     combine_out_dtype: torch.dtype = torch.bfloat16
     weighted_combine: bool = False
@@ -244,7 +251,7 @@ class EpDispatchCombineConfig:
             if f.name in ("data_type", "combine_dtype", "combine_out_dtype"):
                 v = _EP_OF[v]
             elif f.name == "quant_type":
-                v = {"none": EP_QUANT_NONE, "fp8_e4m3_block128": EP_QUANT_FP8_E4M3_BLOCK128}[v]
+                v = _QUANT_OF[v]
             elif f.name in ("combine_impl", "dispatch_impl"):
                 v = {"auto": EP_COMBINE_AUTO, "vector": EP_COMBINE_VECTOR,
                      "bulk": EP_COMBINE_BULK}[v]
@@ -298,9 +305,18 @@ class EpDispatchCombineOp:
             return [T] * R
         return num_tokens
 
-    @property
-    def _dispatch_dtype(self):
-        return torch.float8_e4m3fn if self.config.quant_type != "none" else self.config.data_type
+    def _payload(self):
+        """(dtype, columns) of a received payload row and the number of f32
+        block scales per row (None without quantisation)."""
+        cfg = self.config
+        H = cfg.hidden_dim
+        if cfg.quant_type == "fp8_e4m3_block128":
+            return torch.float8_e4m3fn, H, H // 128
+        if cfg.quant_type == "fp4_e2m1_block32":
+            return torch.uint8, H // 2, H // 32
+        if _FP4X2 is not None and cfg.data_type == _FP4X2:
+            return cfg.data_type, H // 2, None
+        return cfg.data_type, H, None
 
     @staticmethod
     def decode_send_flat_idx(pos: int, world_size: int, max_tokens: int) -> tuple[int, int]:
@@ -319,11 +335,12 @@ class EpDispatchCombineOp:
 
     def _make_dispatch_views(self, o):
         cfg = self.config
-        R, H, k = cfg.world_size, cfg.hidden_dim, cfg.num_experts_per_token
-        x = self._view(o.x, self._dispatch_dtype, (R, self.cap, H))
+        R, k = cfg.world_size, cfg.num_experts_per_token
+        dt, cols, nsc = self._payload()
+        x = self._view(o.x, dt, (R, self.cap, cols))
         if o.scales:
-            if cfg.quant_type != "none":
-                sc = self._view(o.scales, torch.float32, (R, self.cap, H // 128))
+            if nsc is not None:
+                sc = self._view(o.scales, torch.float32, (R, self.cap, nsc))
             else:
                 sc = self._view(o.scales, torch.uint8, (R, self.cap, o.scale_row_bytes))
         else:
@@ -371,10 +388,11 @@ class EpDispatchCombineOp:
     def _std_views(self, o: ep_std_moe_out):
         cfg = self.config
         R, Er, H = cfg.world_size, cfg.num_experts_per_rank, cfg.hidden_dim
+        dt, cols, nsc = self._payload()
         return {
-            "packed_recv_x": self._view(o.packed_x, self._dispatch_dtype, (R, o.pcap, H)),
-            "packed_recv_scales": (self._view(o.packed_scales, torch.float32, (R, o.pcap, H // 128))
-                                   if o.packed_scales and cfg.quant_type != "none" else None),
+            "packed_recv_x": self._view(o.packed_x, dt, (R, o.pcap, cols)),
+            "packed_recv_scales": (self._view(o.packed_scales, torch.float32, (R, o.pcap, nsc))
+                                   if o.packed_scales and nsc is not None else None),
             "packed_recv_count": self._view(o.packed_count, torch.int32, (R, Er)),
             "packed_recv_src_info": self._view(o.packed_src_info, torch.int32, (R, o.pcap)),
             "packed_recv_layout_range": self._view(o.packed_layout_range, torch.int64, (R, Er, R)),

@@ -35,7 +35,7 @@ class Workload:
     tokens_per_rank: int     # max_num_inp_token_per_rank (Tmax)
     hidden: int              # H
     topk: int                # k
-    dispatch_dtype: str      # "bf16" (copy) or "fp8" (fused OCP E4M3 per-128 quant)
+    dispatch_dtype: str      # "bf16" (copy), "fp8" (OCP E4M3 per-128) or "fp4" (E2M1 per-32)
     combine_out_dtype: str   # "bf16" or "fp32"
     router: str = "uniform"  # "uniform" or "zipf"
     zipf_s: float = 1.2
@@ -70,6 +70,10 @@ WORKLOADS: dict[str, Workload] = {
     "skewed_zipf_std_moe": Workload("skewed_zipf_std_moe", 8, 32, 4096, 7168, 8, "bf16", "fp32",
                                     router="zipf", zipf_s=1.2, weighted=True,
                                     standard_moe=True),
+    # the prefill shape with FP4 E2M1 block-32 quantisation in dispatch
+    "ds_v3_throughput_fp4": Workload("ds_v3_throughput_fp4", 8, 32, 4096, 7168, 8, "fp4", "bf16",
+                                     token_dist="normal_outliers", outlier_frac=0.01,
+                                     outlier_scale=50.0),
     # mid-size MoE, 5% of top-k slots dropped, inputs U(-1,1)
     "mid_masked": Workload("mid_masked", 8, 16, 2048, 4096, 8, "bf16", "bf16",
                            mask_prob=0.05, token_dist="uniform"),

@@ -57,7 +57,9 @@ typedef enum {
 typedef enum {
     EP_DTYPE_BF16 = 0,
     EP_DTYPE_FP32 = 1,
-    EP_DTYPE_FP8_E4M3 = 2       /* OCP E4M3 (bias 7, max 448, NaN = S.1111.111) */
+    EP_DTYPE_FP8_E4M3 = 2,      /* OCP E4M3 (bias 7, max 448, NaN = S.1111.111) */
+    EP_DTYPE_FP4_E2M1X2 = 3     /* OCP E2M1 codes, two per byte (even element in the low
+                                   nibble); pre-quantised pass-through, H % 32 == 0 */
 } ep_dtype;
 
 typedef enum {
@@ -80,7 +82,9 @@ typedef enum {
 
 typedef enum {
     EP_QUANT_NONE = 0,          /* dispatch moves the input bits unchanged */
-    EP_QUANT_FP8_E4M3_BLOCK128 = 1  /* bf16 in; E4M3 codes + one f32 scale per 128 elements out */
+    EP_QUANT_FP8_E4M3_BLOCK128 = 1, /* bf16 in; E4M3 codes + one f32 scale per 128 elements out */
+    EP_QUANT_FP4_E2M1_BLOCK32 = 2   /* bf16 in; packed E2M1 codes (H/2 bytes) + one f32 scale
+                                       (amax / 6) per 32 elements out; H % 32 == 0 */
 } ep_quant;
 
 /*
@@ -91,7 +95,7 @@ typedef struct ep_config {
     int32_t world_size;                  /* simulated EP ranks, 1..EP_MAX_WORLD_SIZE */
     int32_t hidden_dim;                  /* H, elements per token */
     int32_t scale_dim;                   /* pass-through scales per token (0 = none); with
-                                            FP8 quantisation 0 or H/128 (then 4-byte) */
+                                            FP8 (FP4) quantisation 0 or H/128 (H/32), 4-byte */
     int32_t scale_type_size;             /* bytes per pass-through scale element */
     int32_t max_token_type_size;         /* bytes of the widest combine element (2 or 4) */
     int32_t max_num_inp_token_per_rank;  /* Tmax */

@@ -57,6 +57,10 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_e4m3_from_f32_array.argtypes = [P, L, P]
         _lib.oracle_bf16_from_f32_array.argtypes = [P, L, P]
         _lib.oracle_quant_tokens.argtypes = [L, I, P, P, P]
+        _lib.oracle_quant_tokens_fp4.argtypes = [L, I, P, P, P]
+        _lib.oracle_e2m1_from_f32_array.argtypes = [P, L, P]
+        _lib.oracle_e2m1_to_f32.restype = ctypes.c_float
+        _lib.oracle_e2m1_to_f32.argtypes = [ctypes.c_uint8]
         _lib.oracle_route.argtypes = [I, I, I, I, P, P, P, P, P]
         _lib.oracle_place_rows.argtypes = [I, I, L, P, P, P, P]
         _lib.oracle_combine.argtypes = [I, I, I, I, I, P, P, P, I, P, P, I, I, P, P]
@@ -118,6 +122,31 @@ def e4m3_to_f32(c: np.ndarray) -> np.ndarray:
     return table[c]
 
 
+def e2m1_from_f32(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().oracle_e2m1_from_f32_array(_p(v), v.size, _p(out))
+    return out
+
+
+def e2m1_to_f32(c: np.ndarray) -> np.ndarray:
+    c = np.asarray(c, np.uint8)
+    table = np.array([lib().oracle_e2m1_to_f32(i) for i in range(16)], np.float32)
+    return table[c & 0xF]
+
+
+def quant_tokens_fp4(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """x uint16 [..., H] -> (packed E2M1 uint8 [..., H/2], scales f32 [..., H/32])."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    H = x.shape[-1]
+    assert H % 32 == 0
+    n = x.size // H
+    q = np.empty(x.shape[:-1] + (H // 2,), np.uint8)
+    sc = np.empty(x.shape[:-1] + (H // 32,), np.float32)
+    lib().oracle_quant_tokens_fp4(n, H, _p(x), _p(q), _p(sc))
+    return q, sc
+
+
 def quant_tokens(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     """x uint16 [..., H] -> (codes uint8 [..., H], scales f32 [..., H/128])."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
@@ -157,7 +186,8 @@ def place_rows(rows: np.ndarray, ntok: np.ndarray, slot: np.ndarray) -> np.ndarr
 
 
 def dispatch(x: np.ndarray, w: np.ndarray, idx: np.ndarray, ntok: np.ndarray,
-             experts_per_rank: int, quant_fp8: bool = False, scales: np.ndarray | None = None):
+             experts_per_rank: int, quant_fp8: bool = False, scales: np.ndarray | None = None,
+             quant_fp4: bool = False):
     """Full 2D dispatch. x: uint16 bf16 bits or uint8 fp8 codes [R, Tmax, H].
 
     Returns a dict with recv_num_token, src_pos, slot, x, w, idx, scales
@@ -166,8 +196,8 @@ def dispatch(x: np.ndarray, w: np.ndarray, idx: np.ndarray, ntok: np.ndarray,
     """
     recv, src_pos, slot = route(idx, ntok, experts_per_rank)
     out = {"recv_num_token": recv, "src_pos": src_pos, "slot": slot}
-    if quant_fp8:
-        q, sc = quant_tokens(x)
+    if quant_fp8 or quant_fp4:
+        q, sc = quant_tokens(x) if quant_fp8 else quant_tokens_fp4(x)
         out["x"] = place_rows(q, ntok, slot)
         out["scales"] = place_rows(sc, ntok, slot)
     else:

@@ -41,6 +41,9 @@
  *   R8 standard-MoE combine: ranks ascending, then slots ascending, fmaf(w_j, y, acc).
  *   R9 convert_combine_input: per (token, rank) the unweighted fp32 sum of that token's
  *      expert rows on the rank, slots ascending, rounded once to the output dtype.
+ *   R10 FP4: OCP E2M1 codes (bias 1, 1 mantissa bit, max 6, no Inf/NaN), one f32 scale per
+ *      32-element block, scale = amax / 6, code = E2M1_RNE_sat(x / scale) (amax == 0: enc(x));
+ *      two codes per byte, the even element in the low nibble.
  */
 #include <math.h>
 #include <stdint.h>
@@ -118,6 +121,40 @@ void oracle_bf16_from_f32_array(const float* v, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_from_f32(v[i]);
 }
 
+/* [OCP] E2M1 (FP4): 1 sign, 2 exponent bits (bias 1), 1 mantissa bit; no
+ * infinities or NaN; magnitudes 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6.
+ * Round to nearest with ties to the even code, then saturate to +-6. */
+uint8_t oracle_e2m1_from_f32(float v) {
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    if (isnan(v)) return 0x7;                /* no NaN code: saturate (never generated) */
+    double a = fabs((double)v);
+    if (a >= 6.0) return (uint8_t)(sign | 0x7);
+    if (a == 0.0) return sign;
+    int e2;
+    (void)frexp(a, &e2);
+    int ue = e2 - 1;                         /* a in [2^ue, 2^(ue+1)) */
+    if (ue < 0) ue = 0;                      /* subnormal 0.5 shares the spacing of [1, 2) */
+    double quantum = ldexp(1.0, ue - 1);     /* one mantissa bit */
+    double q = rint(a / quantum) * quantum;  /* ties to even */
+    if (q > 6.0) return (uint8_t)(sign | 0x7);
+    if (q == 0.0) return sign;
+    if (q < 1.0) return (uint8_t)(sign | 0x1); /* 0.5 */
+    (void)frexp(q, &e2);
+    int E = (e2 - 1) + 1;
+    int M = (int)(q / ldexp(1.0, e2 - 1) * 2.0) - 2;
+    return (uint8_t)(sign | (E << 1) | M);
+}
+
+float oracle_e2m1_to_f32(uint8_t c) {
+    int s = (c >> 3) & 1, E = (c >> 1) & 3, M = c & 1;
+    double v = (E == 0) ? M * 0.5 : (1.0 + M / 2.0) * ldexp(1.0, E - 1);
+    return (float)(s ? -v : v);
+}
+
+void oracle_e2m1_from_f32_array(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_from_f32(v[i]);
+}
+
 static float load_elem(int dtype, const void* base, int64_t i) {
     if (dtype == DT_BF16) return oracle_bf16_to_f32(((const uint16_t*)base)[i]);
     return ((const float*)base)[i];
@@ -152,6 +189,32 @@ void oracle_quant_row(int H, const uint16_t* x, uint8_t* q, float* scales) {
 void oracle_quant_tokens(int64_t n, int H, const uint16_t* x, uint8_t* q, float* scales) {
     for (int64_t i = 0; i < n; ++i)
         oracle_quant_row(H, x + i * H, q + i * H, scales + i * (H / 128));
+}
+
+/* Reading R10: one token row of H bf16 values -> H/2 bytes of packed E2M1
+ * codes and H/32 f32 scales. */
+void oracle_quant_row_fp4(int H, const uint16_t* x, uint8_t* q, float* scales) {
+    for (int b = 0; b < H / 32; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float a = fabsf(oracle_bf16_to_f32(x[b * 32 + i]));
+            if (a > amax) amax = a;
+        }
+        float scale = amax / 6.0f;
+        scales[b] = scale;
+        for (int i = 0; i < 32; i += 2) {
+            float v0 = oracle_bf16_to_f32(x[b * 32 + i]);
+            float v1 = oracle_bf16_to_f32(x[b * 32 + i + 1]);
+            uint8_t c0 = (amax == 0.0f) ? oracle_e2m1_from_f32(v0) : oracle_e2m1_from_f32(v0 / scale);
+            uint8_t c1 = (amax == 0.0f) ? oracle_e2m1_from_f32(v1) : oracle_e2m1_from_f32(v1 / scale);
+            q[(b * 32 + i) / 2] = (uint8_t)(c0 | (c1 << 4));
+        }
+    }
+}
+
+void oracle_quant_tokens_fp4(int64_t n, int H, const uint16_t* x, uint8_t* q, float* scales) {
+    for (int64_t i = 0; i < n; ++i)
+        oracle_quant_row_fp4(H, x + i * H, q + i * (H / 2), scales + i * (H / 32));
 }
 
 /* ------------------------------------------------------- routing layout */

@@ -36,7 +36,8 @@ def make_config(wl, **over) -> EpDispatchCombineConfig:
         data_type=torch.bfloat16, world_size=wl.world_size, hidden_dim=wl.hidden, scale_dim=0,
         scale_type_size=4, max_token_type_size=4, max_num_inp_token_per_rank=wl.tokens_per_rank,
         num_experts_per_rank=wl.experts_per_rank, num_experts_per_token=wl.topk,
-        quant_type="fp8_e4m3_block128" if wl.dispatch_dtype == "fp8" else "none",
+        quant_type={"fp8": "fp8_e4m3_block128", "fp4": "fp4_e2m1_block32"}.get(wl.dispatch_dtype,
+                                                                            "none"),
         combine_dtype=torch.bfloat16,
         combine_out_dtype=torch.float32 if wl.combine_out_dtype == "fp32" else torch.bfloat16,
         weighted_combine=wl.weighted, standard_moe=wl.standard_moe)
@@ -63,6 +64,13 @@ class Inputs:
             return bits16(self.x)
         s, t = rows
         return bits16(self.x[torch.as_tensor(s, device=DEV), torch.as_tensor(t, device=DEV)])
+
+
+def oracle_quant(cfg, xb: np.ndarray):
+    """The oracle's codes and block scales for the config's quantisation."""
+    if cfg.quant_type == "fp8_e4m3_block128":
+        return oracle.quant_tokens(xb)
+    return oracle.quant_tokens_fp4(xb)
 
 
 def check_route(inp: Inputs, recv_d, src_pos_d):

@@ -13,8 +13,8 @@ import oracle
 from combine_route_layout_gb300 import EpDispatchCombineOp, EpError
 from combine_route_layout_gb300 import ep as E
 from gen import WORKLOADS, make_expert_outputs
-from ep_harness import (DEV, Inputs, bits16, check_route, host, make_config, sample_rows,
-                        sample_tokens)
+from ep_harness import (DEV, Inputs, bits16, check_route, host, make_config, oracle_quant,
+                        sample_rows, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ def run_2d(wl, seed=None, ragged=False, full=True, nsample=192, cfg_over=None,
     if full:
         xb = inp.x_bits()
         if quant:
-            q, sc = oracle.quant_tokens(xb)
+            q, sc = oracle_quant(cfg, xb)
             x_ref, sc_ref = oracle.place_rows(q, inp.ntok, slot), oracle.place_rows(sc, inp.ntok, slot)
         else:
             x_ref, sc_ref = oracle.place_rows(xb, inp.ntok, slot), None
@@ -69,7 +69,7 @@ def run_2d(wl, seed=None, ragged=False, full=True, nsample=192, cfg_over=None,
         xb = inp.x_bits((st[:, 0], st[:, 1]))
         gx = host(d_x[torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
         if quant:
-            q, sc = oracle.quant_tokens(xb)
+            q, sc = oracle_quant(cfg, xb)
             gsc = host(d_sc[torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
             assert np.array_equal(gx, q), "sampled FP8 codes"
             assert np.array_equal(gsc.view(np.uint32), sc.view(np.uint32)), "sampled scales"
@@ -261,7 +261,7 @@ def run_std(wl, seed=None, ragged=False, full=True, nsample=256, cfg_over=None):
     xb = inp.x_bits((st[:, 0], st[:, 1]))
     gx = host(v["packed_recv_x"][torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
     if quant:
-        q, sc = oracle.quant_tokens(xb)
+        q, sc = oracle_quant(cfg, xb)
         gsc = host(v["packed_recv_scales"][torch.as_tensor(rr, device=DEV),
                                            torch.as_tensor(ii, device=DEV)])
         assert np.array_equal(gx, q)
@@ -694,3 +694,111 @@ def test_bulk_dispatch_fp8_passthrough_with_scales():
 def test_bulk_dispatch_full_size():
     run_2d(WORKLOADS["mid_masked"], full=False, cfg_over=dict(dispatch_impl="bulk"))
     run_std(WORKLOADS["skewed_zipf_std_moe"], full=False, cfg_over=dict(dispatch_impl="bulk"))
+
+
+# --------------------------------------------------------------- FP4 dispatch
+
+@pytest.mark.parametrize("over,seed", [(dict(), 0), (dict(tokens_per_rank=300, hidden=1056), 1),
+                                       (dict(tokens_per_rank=70, hidden=224), 2)])
+def test_fp4_dispatch(over, seed):
+    """FP4 E2M1 block-32 quantisation in dispatch: codes, nibble order and
+    scales bit-exact against the oracle (2D layout)."""
+    wl = WORKLOADS["ds_v3_latency"].with_(dispatch_dtype="fp4").with_(**over)
+    run_2d(wl, seed=seed, ragged=bool(seed))
+
+
+def test_fp4_dispatch_standard_moe():
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=150, hidden=1024,
+                                               dispatch_dtype="fp4")
+    run_std(wl, seed=3, ragged=True)
+
+
+def test_fp4_quant_signed_zero_blocks():
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=8, hidden=256, dispatch_dtype="fp4")
+    inp = Inputs(wl, 4)
+    x = inp.x.clone()
+    x[0, 0, :32] = 0.0
+    x[0, 1, 32:64] = -0.0
+    x[1, 2, :32] = torch.tensor(1e-38).to(torch.bfloat16)
+    inp.x = x
+    op = EpDispatchCombineOp(make_config(wl))
+    d_x, _, d_sc, _, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    q, sc = oracle.quant_tokens_fp4(bits16(x))
+    x_ref, sc_ref = oracle.place_rows(q, inp.ntok, slot), oracle.place_rows(sc, inp.ntok, slot)
+    gx, gs = host(d_x), host(d_sc)
+    for r in range(wl.world_size):
+        n = recv[r]
+        assert np.array_equal(gx[r, :n], x_ref[r, :n])
+        assert np.array_equal(gs[r, :n].view(np.uint32), sc_ref[r, :n].view(np.uint32))
+    op.reset()
+
+
+def test_fp4_quotients_on_e2m1_midpoints():
+    """As the E4M3 midpoint test, for FP4: blocks of 32 with amax 6*c, the
+    other elements c times an E2M1 midpoint (0.25 sits on a binade start) or
+    one bf16 step away."""
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=40, hidden=1024, dispatch_dtype="fp4")
+    R, T, H = wl.world_size, wl.tokens_per_rank, wl.hidden
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    mids = np.concatenate([(mags[1:] + mags[:-1]) / 2, mags])
+    mults = np.array([3, 5, 7, 0.75, 1.5, 2.5, 3.5, 0.375, 1.25, 96, 0.0234375, 6], np.float64)
+    rng = np.random.default_rng(21)
+    x = np.empty((R, T, H), np.float32)
+    for s in range(R):
+        for t in range(T):
+            for b in range(H // 32):
+                c = mults[rng.integers(len(mults))]
+                blk = c * rng.choice(mids, size=32) * rng.choice([-1.0, 1.0], size=32)
+                blk[rng.integers(32)] = 6.0 * c * rng.choice([-1.0, 1.0])
+                x[s, t, b * 32:(b + 1) * 32] = blk
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    nudge = rng.random(xb.shape) < 0.2
+    xi = xb.view(torch.int16)
+    xi[torch.from_numpy(nudge)] += torch.from_numpy(rng.choice([-1, 1], size=int(nudge.sum()))
+                                                    ).to(torch.int16)
+    inp = Inputs(wl, 0)
+    inp.x = xb.to(DEV)
+    op = EpDispatchCombineOp(make_config(wl))
+    d_x, d_w, d_sc, _, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    q, sc = oracle.quant_tokens_fp4(bits16(xb))
+    x_ref, sc_ref = oracle.place_rows(q, inp.ntok, slot), oracle.place_rows(sc, inp.ntok, slot)
+    gx, gsc = host(d_x), host(d_sc)
+    for r in range(R):
+        n = recv[r]
+        assert np.array_equal(gsc[r, :n].view(np.uint32), sc_ref[r, :n].view(np.uint32))
+        assert np.array_equal(gx[r, :n], x_ref[r, :n]), f"codes rank {r}"
+    op.reset()
+
+
+def test_cuda_graph_replay_bulk_paths():
+    """Graph capture and replay with the bulk-copy dispatch and combine (chosen
+    automatically from 8192 tokens on), compared with the oracle."""
+    wl = WORKLOADS["mid_masked"].with_(tokens_per_rank=1024, hidden=1024)
+    R, T = wl.world_size, wl.tokens_per_rank
+    inp = Inputs(wl, 2)
+    op = EpDispatchCombineOp(make_config(wl))
+    y = make_expert_outputs(wl, R * T, 2, device=DEV)
+    out = torch.empty((R, T, wl.hidden), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, None)
+        op.combine(y, d[1], None, out=out, call_reset=True)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, None)
+        op.combine(y, d[1], None, out=out, call_reset=True)
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    op.sync()
+    recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, wl.experts_per_rank)
+    ref, _ = oracle.combine(host(y), inp.idx, inp.ntok, slot, wl.experts_per_rank, out_dtype="bf16")
+    assert np.array_equal(host(out), ref)

@@ -490,3 +490,57 @@ def test_pins_detect_planted_mistakes(oracle_lib):
     x = xb.float().numpy().reshape(-1)
     dec = oracle_lib.e4m3_to_f32(q.reshape(-1) ^ 0x80).astype(np.float64) * np.repeat(sc.ravel(), 128)
     assert np.any(np.abs(dec - x) > 2.0**-4 * np.abs(x) + 2.0**-10 * np.repeat(sc.ravel(), 128))
+
+
+# ------------------------------------------------------------------- FP4
+
+def test_e2m1_golden_values(oracle_lib):
+    for expr, code in _read_golden("e2m1_ocp_values.txt"):
+        v = np.float32(eval(expr, {"__builtins__": {}}))
+        assert int(oracle_lib.e2m1_from_f32(np.array([v]))[0]) == int(code, 16), expr
+    mags = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert list(oracle_lib.e2m1_to_f32(np.arange(8))) == mags
+    assert list(oracle_lib.e2m1_to_f32(np.arange(8, 16))) == [-m for m in mags]
+
+
+def test_e2m1_encode_vs_brute_force(oracle_lib):
+    rng = np.random.default_rng(12)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    mids = (mags[1:] + mags[:-1]) / 2
+    v = np.concatenate([mags, mids, np.nextafter(mids.astype(np.float32), np.float32(9)),
+                        np.nextafter(mids.astype(np.float32), np.float32(-1)),
+                        rng.random(20000) * 8]).astype(np.float32)
+    v = np.concatenate([v, -v])
+    got = oracle_lib.e2m1_from_f32(v)
+    for x, c in zip(v.astype(np.float64), got):
+        d = np.abs(mags - abs(x))
+        tied = np.nonzero(d == d.min())[0]
+        m = tied[(tied & 1) == 0][0] if len(tied) > 1 else tied[0]
+        assert c == (m | (8 if np.signbit(x) else 0)), (x, c)
+
+
+def test_fp4_quant_invariants(oracle_lib):
+    wl = WORKLOADS["ds_v3_throughput"].with_(tokens_per_rank=6, world_size=2, hidden=1024)
+    xb = make_tokens(wl, seed=13)
+    xb[0, 0, :32] = 0.0
+    xb[0, 1, 32:64] = -0.0
+    q, sc = oracle_lib.quant_tokens_fp4(_bits(xb))
+    assert q.shape[-1] == 512 and sc.shape[-1] == 32
+    x = xb.float().numpy().reshape(-1)
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(-1)   # even element in the low nibble
+    s = np.repeat(sc.reshape(-1).astype(np.float64), 32)
+    # every code is the encoder's code of x / scale (or of x when the block is all zero)
+    v = np.where(s == 0, x, x / np.where(s == 0, 1, s).astype(np.float32))
+    assert np.array_equal(codes, oracle_lib.e2m1_from_f32(v.astype(np.float32)))
+    # the element of largest magnitude in each block encodes to +-6
+    xb32 = x.reshape(-1, 32)
+    top = codes.reshape(-1, 32)[np.arange(len(xb32)), np.abs(xb32).argmax(1)]
+    nz = np.abs(xb32).max(1) > 0
+    assert np.all((top[nz] & 7) == 7)
+    nblk = 1024 // 32                                    # blocks per token
+    assert np.all(codes.reshape(-1, 32)[0] == 0) and np.all(codes.reshape(-1, 32)[nblk + 1] == 8)
+    # E2M1 error bound: half a code step in units of the scale
+    dec = oracle_lib.e2m1_to_f32(codes).astype(np.float64) * s
+    a = np.abs(x) / np.where(s == 0, 1, s)
+    step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    assert np.all(np.abs(dec - x) <= 0.5 * step * s * (1 + 1e-6) + 1e-30)
