@@ -107,7 +107,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -461,7 +461,9 @@ def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
     steps, warm = args.steps, args.warmup
-    T = args.ref_tokens
+    # per-step sample: --ref-tokens tokens/rank, shrunk so that all steps take
+    # about two minutes of oracle time at most (~3.5 ms per token/rank per step)
+    T = max(8, min(args.ref_tokens, int(120.0 / (0.0035 * (steps + warm)))))
     y = None
     for _ in range(warm):
         _, _, y = cpu_oracle_step(wl, T, y=y)
@@ -479,7 +481,8 @@ def run_reference(args, wl, rank, world):
         "config": {"workload": wl.name, "sample_tokens_per_rank": T, "world_size": wl.world_size,
                    "experts_per_rank": wl.experts_per_rank, "hidden": wl.hidden, "topk": wl.topk},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{T} tokens/rank per step, single-threaded C oracle"},
+                         "sample": f"{wl.name} restricted to {T} tokens/rank per step, "
+                                   f"single-threaded C oracle, {tot:.1f} s over {steps} steps"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -490,7 +493,7 @@ def run_reference(args, wl, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ds_v3_throughput", choices=sorted(WORKLOADS))
@@ -615,11 +618,13 @@ def main():
         del ls, flush
 
     if not args.no_e2e:
-        e_ms, h2d, d2h = time_e2e(step, K, args.warmup, barrier)
+        ke = min(K, 20)  # host-link bound (~18 ms a step): a few steps suffice
+        e_ms, h2d, d2h = time_e2e(step, ke, args.warmup, barrier)
         e_ms = reduce_max(e_ms, world)
-        line["e2e"] = {"value": round(step_bytes * world / (e_ms / K * 1e-3) / 1e9, 2),
+        line["e2e"] = {"value": round(step_bytes * world / (e_ms / ke * 1e-3) / 1e9, 2),
                        "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-                       "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / K, 3)}
+                       "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / ke, 3),
+                       "steps": ke}
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_tokens, args.cpu_reps)
     if rank == 0:
