@@ -347,7 +347,7 @@ ep_status check_dispatch_inputs(ep_handle* h, const void* x, const float* w, con
   if (!aligned(w, 4) || !aligned(idx, 4))
     return fail(EP_ERR_INVALID_ARG, "weights and indices must be 4-byte aligned");
   if (h->g.quant && scales)
-    return fail(EP_ERR_INVALID_ARG, "scales must be NULL with FP8 block quantisation");
+    return fail(EP_ERR_INVALID_ARG, "scales must be NULL with block quantisation (computed)");
   if (!h->g.quant && h->g.in_scale_row_bytes > 0 && !scales)
     return fail(EP_ERR_INVALID_ARG, "scale_dim > 0 needs a scales array");
   if (scales && (h->g.in_scale_row_bytes % 4 == 0) && !aligned(scales, 4))
