@@ -530,6 +530,9 @@ def main():
         line = run_reference(args, wl, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     dev = torch.device("cuda", local)

@@ -802,3 +802,80 @@ def test_cuda_graph_replay_bulk_paths():
     recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, wl.experts_per_rank)
     ref, _ = oracle.combine(host(y), inp.idx, inp.ntok, slot, wl.experts_per_rank, out_dtype="bf16")
     assert np.array_equal(host(out), ref)
+
+
+# ----------------------------------------------------------- more dtypes
+
+def test_fp32_input_copy_dispatch():
+    """f32 tokens pass through dispatch bit for bit (copy mode), vector and bulk kernels."""
+    wl = WORKLOADS["tiny"].with_(tokens_per_rank=300, hidden=520)
+    R, T, H = wl.world_size, wl.tokens_per_rank, wl.hidden
+    inp = Inputs(wl, 3, ragged=True)
+    x = torch.randn((R, T, H), device=DEV, dtype=torch.float32)
+    for impl in ("vector", "bulk"):
+        op = EpDispatchCombineOp(make_config(wl, data_type=torch.float32, dispatch_impl=impl))
+        d_x, d_w, _, d_idx, recv_d = op.dispatch(x, inp.w_d, None, inp.idx_d, inp.ntok)
+        op.sync()
+        recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+        ref = oracle.place_rows(host(x), inp.ntok, slot)
+        gx = host(d_x)
+        for r in range(R):
+            assert np.array_equal(gx[r, :recv[r]].view(np.uint32), ref[r, :recv[r]].view(np.uint32))
+        op.reset()
+
+
+def test_fp4_passthrough_with_scales():
+    """Pre-quantised FP4 payloads (two E2M1 codes per byte) and their scales
+    pass through dispatch unchanged."""
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    if fp4 is None:
+        pytest.skip("torch has no packed FP4 dtype")
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=70, hidden=1024)
+    R, T, H = wl.world_size, wl.tokens_per_rank, wl.hidden
+    inp = Inputs(wl, 8, ragged=True)
+    packed = torch.randint(0, 256, (R, T, H // 2), dtype=torch.uint8, device=DEV)
+    scales = torch.rand((R, T, H // 32), device=DEV, dtype=torch.float32)
+    op = EpDispatchCombineOp(make_config(wl, data_type=fp4, quant_type="none",
+                                         scale_dim=H // 32, scale_type_size=4))
+    d_x, d_w, d_sc, d_idx, recv_d = op.dispatch(packed.view(fp4), inp.w_d, scales, inp.idx_d,
+                                                inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    x_ref = oracle.place_rows(host(packed), inp.ntok, slot)
+    sc_ref = oracle.place_rows(host(scales), inp.ntok, slot)
+    gx = d_x.contiguous().view(torch.uint8).cpu().numpy()
+    gs = host(d_sc).view(np.float32)
+    for r in range(R):
+        n = recv[r]
+        assert np.array_equal(gx[r, :n], x_ref[r, :n])
+        assert np.array_equal(gs[r, :n].reshape(n, -1).view(np.uint32), sc_ref[r, :n].view(np.uint32))
+    op.reset()
+
+
+@pytest.mark.parametrize("quant", ["fp8", "fp4"])
+def test_convert_dispatch_output_carries_quantised_rows(quant):
+    """convert_dispatch_output after a quantising dispatch carries codes and
+    block scales into the packed layout, equal to the fused packed dispatch."""
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=140, hidden=1024, mask_prob=0.1,
+                                               dispatch_dtype=quant)
+    R, T, Er = wl.world_size, wl.tokens_per_rank, wl.experts_per_rank
+    inp = Inputs(wl, 5, ragged=True)
+    cfg = make_config(wl, standard_moe=True)
+    op = EpDispatchCombineOp(cfg)
+    d_x, d_w, d_sc, d_idx, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    o = E.ep_convert_dispatch_output(op._handle, d_x.data_ptr(), d_idx.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream)
+    v = op._std_views(o)
+    op.sync()
+    q, sc = oracle_quant(cfg, inp.x_bits())
+    ref = oracle.std_layout(inp.idx, inp.ntok, Er, o.pcap)
+    px_ref = oracle.std_place_rows(q, inp.ntok, ref["row_map"], o.pcap)
+    ps_ref = oracle.std_place_rows(sc, inp.ntok, ref["row_map"], o.pcap)
+    gx, gs, gsi = host(v["packed_recv_x"]), host(v["packed_recv_scales"]), host(v["packed_recv_src_info"])
+    for r in range(R):
+        n = ref["rank_rows"][r]
+        used = ref["src_info"][r, :n] >= 0
+        assert np.array_equal(gsi[r, :n], ref["src_info"][r, :n])
+        assert np.array_equal(gx[r, :n][used], px_ref[r, :n][used])
+        assert np.array_equal(gs[r, :n][used].view(np.uint32), ps_ref[r, :n][used].view(np.uint32))
+    op.reset()
