@@ -446,8 +446,6 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
   lp.chunk_cnt = h->w.chunk_cnt2d;
   lp.chunk_off = h->w.chunk_off2d;
   lp.ticket = h->w.tickets + 0;
-  cudaError_t e = ep::launch_layout_2d(lp, st);
-  if (e != cudaSuccess) return cuda_fail(e, "routing-layout launch");
 
   ep::DispatchParams dp;
   fill_dispatch_common(h, x, weights, scales, indices, &dp);
@@ -462,9 +460,18 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
   dp.out_w = h->w.recv_w;
   dp.out_idx = h->w.recv_idx;
   dp.err = h->w.err;
-  e = use_bulk_dispatch(h, dp)
-          ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h), st)
-          : ep::launch_dispatch_2d(dp, h->g.quant ? h->cfg.quant_type : 0, launch_cfg(h), st);
+  const bool bulk = use_bulk_dispatch(h, dp);
+  if (!bulk && h->g.nchunks <= ep::kSmallScanChunks) {
+    // small batch: the vector dispatch kernel sums the (few) chunk counts
+    // itself, which takes the layout's last-CTA scan off the critical path
+    lp.no_scan = 1;
+    dp.chunk_cnt = h->w.chunk_cnt2d;
+    dp.recv_num_token = h->w.recv_num_token;
+  }
+  cudaError_t e = ep::launch_layout_2d(lp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "routing-layout launch");
+  e = bulk ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h), st)
+           : ep::launch_dispatch_2d(dp, h->g.quant ? h->cfg.quant_type : 0, launch_cfg(h), st);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
 
   h->state = kDispatched;

@@ -26,9 +26,22 @@ __device__ __forceinline__ int slot_on_lane_rank(const DispatchParams& p, int64_
                                                  uint32_t m, int lane) {
   if (lane < p.R && ((m >> lane) & 1u)) {
     const int c = s * p.cpr + t / kChunk;
-    return __ldg(p.chunk_off + (int64_t)c * p.R + lane) + (int)__ldg(p.local8 + g * p.R + lane);
+    const int local = __ldg(p.local8 + g * p.R + lane);
+    if (!p.chunk_cnt) return __ldg(p.chunk_off + (int64_t)c * p.R + lane) + local;
+    int off = 0;  // small batch: at most kSmallScanChunks - 1 earlier chunks
+#pragma unroll 4
+    for (int cc = 0; cc < c; ++cc) off += __ldg(p.chunk_cnt + (int64_t)cc * p.R + lane);
+    return off + local;
   }
   return -1;
+}
+
+// Small batches: recv_num_token from the chunk counts (CTA 0, after the layout).
+__device__ __forceinline__ void recv_from_counts(const DispatchParams& p) {
+  if (!p.chunk_cnt || blockIdx.x != 0 || (int)threadIdx.x >= p.R) return;
+  int n = 0;
+  for (int cc = 0; cc < p.R * p.cpr; ++cc) n += __ldg(p.chunk_cnt + (int64_t)cc * p.R + threadIdx.x);
+  p.recv_num_token[threadIdx.x] = n;
 }
 
 // Packed row (global index r*pcap + row) of slot `lane` (standard MoE), or -1.
@@ -151,6 +164,7 @@ __global__ void __launch_bounds__(256, 4) dispatch_copy_kernel(DispatchParams p)
     }
   }
   pdl_wait();  // never finish before the routing layout, even with no work
+  if (!STD) recv_from_counts(p);
 }
 
 // ------------------------------------------------------------ FP8 quant mode
@@ -287,6 +301,7 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
     }
   }
   pdl_wait();  // never finish before the routing layout, even with no work
+  if (!STD) recv_from_counts(p);
 }
 
 template <bool STD>

@@ -45,6 +45,7 @@ struct LayoutParams {
   int32_t* chunk_off;         // exclusive prefix over chunks, same shape
   unsigned int* ticket;       // last-CTA election counter (returns to 0)
   int32_t* err;
+  int no_scan = 0;            // 2D: leave chunk_off and recv_num_token to the dispatch kernel
 };
 
 struct DispatchParams {
@@ -76,7 +77,14 @@ struct DispatchParams {
   float* out_w;                // 2D only
   int32_t* out_idx;            // 2D only
   int32_t* err;
+  // 2D, small batches (layout run with no_scan): a token's chunk offset is the
+  // sum of the earlier chunks' counts, and CTA 0 writes recv_num_token
+  const int32_t* chunk_cnt = nullptr;
+  int32_t* recv_num_token = nullptr;
 };
+
+// Largest chunk count for which the dispatch kernel sums chunk counts itself.
+constexpr int kSmallScanChunks = 16;
 
 struct CombineParams {
   int R, Tmax, k, E_r, H;

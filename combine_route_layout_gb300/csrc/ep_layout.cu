@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_2d_kernel(LayoutParams 
     if ((m >> r) & 1u) p.local8[g * p.R + r] = (uint8_t)(wpre[warp][r] + __popc(b & lt));
   }
 
+  if (p.no_scan) return;  // small batch: the dispatch kernel sums the chunk counts
   if (!elect_last_cta(p.ticket)) return;
   // Last CTA: one warp per destination rank scans that rank's chunk counts
   // (each lane a contiguous run of chunks), all ranks in parallel.

@@ -879,3 +879,22 @@ def test_convert_dispatch_output_carries_quantised_rows(quant):
         assert np.array_equal(gx[r, :n][used], px_ref[r, :n][used])
         assert np.array_equal(gs[r, :n][used].view(np.uint32), ps_ref[r, :n][used].view(np.uint32))
     op.reset()
+
+
+# ------------------------------------------ small batches: summed chunk counts
+
+@pytest.mark.parametrize("name,over,seed", [
+    ("ds_v3_latency", dict(tokens_per_rank=512, hidden=1024), 4),    # 16 chunks: summed counts
+    ("ds_v3_latency", dict(tokens_per_rank=513, hidden=1024), 5),    # 24 chunks: scanned offsets
+    ("ds_v3_latency", dict(tokens_per_rank=257, hidden=1024, dispatch_dtype="fp4"), 6),
+    ("ds_v3_latency", dict(dispatch_dtype="bf16", hidden=1032), 7),
+    ("tiny", dict(world_size=1, experts_per_rank=8, topk=4, tokens_per_rank=4096), 8),
+    ("tiny", dict(world_size=16, experts_per_rank=2, topk=8, tokens_per_rank=256), 9),
+    ("mid_masked", dict(tokens_per_rank=200, mask_prob=0.5, hidden=1024), 10),
+])
+def test_small_batch_chunk_offsets(name, over, seed):
+    """Up to 16 routing chunks the dispatch kernel adds up the earlier chunks'
+    counts itself (the layout skips its offset scan) and writes
+    recv_num_token; beyond that the layout's scanned offsets are used. Both
+    against the oracle, ragged token counts included."""
+    run_2d(WORKLOADS[name].with_(**over), seed=seed, ragged=True)
