@@ -898,3 +898,62 @@ def test_small_batch_chunk_offsets(name, over, seed):
     recv_num_token; beyond that the layout's scanned offsets are used. Both
     against the oracle, ragged token counts included."""
     run_2d(WORKLOADS[name].with_(**over), seed=seed, ragged=True)
+
+
+# ------------------------------- quantisation with arbitrary (inexact) scales
+
+def _quant_sweep(fmt, amax_bits):
+    """Every finite bf16 value with |x| <= amax in blocks whose amax is fixed,
+    for each amax in amax_bits: codes and scales from dispatch against the
+    oracle's encoder, bit for bit."""
+    blk = 128 if fmt == "fp8" else 32
+    per = blk - 1
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (allb.astype(np.uint32) << 16).view(np.float32)
+    rows = []
+    for ab in amax_bits:
+        amax = float((np.uint32(ab) << np.uint32(16)).view(np.float32))
+        keep = np.isfinite(vals) & (np.abs(vals) <= amax)
+        bits = allb[keep]
+        nblk = -(-len(bits) // per)
+        b = np.zeros((nblk, blk), np.uint16)
+        b[:, per] = ab
+        flat = b[:, :per].reshape(-1)
+        flat[:len(bits)] = bits
+        b[:, :per] = flat.reshape(nblk, per)
+        rows.append(b)
+    x = np.concatenate(rows).reshape(-1)
+    H = 1024
+    T = -(-x.size // H)
+    xx = np.zeros(T * H, np.uint16)
+    xx[:x.size] = x
+    x = xx.reshape(1, T, H)
+    wl = WORKLOADS["tiny"].with_(world_size=1, experts_per_rank=1, topk=1, tokens_per_rank=T,
+                                 hidden=H, dispatch_dtype=fmt, expert_output="random")
+    op = EpDispatchCombineOp(make_config(wl))
+    xd = torch.from_numpy(x.view(np.int16)).to(DEV).view(torch.bfloat16)
+    w = torch.ones((1, T, 1), dtype=torch.float32, device=DEV)
+    idx = torch.zeros((1, T, 1), dtype=torch.int32, device=DEV)
+    d_x, _, d_sc, _, _ = op.dispatch(xd, w, None, idx, [T])
+    op.sync()
+    q_ref, sc_ref = (oracle.quant_tokens if fmt == "fp8" else oracle.quant_tokens_fp4)(x)
+    assert np.array_equal(host(d_sc)[0, :T].view(np.uint32), sc_ref[0].view(np.uint32))
+    assert np.array_equal(host(d_x)[0, :T], q_ref[0])
+    op.reset()
+
+
+def _bf16_bits(v):
+    return int((np.array([v], np.float32).view(np.uint32)[0] + 0x8000) >> 16)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+def test_quant_codes_every_bf16_value_inexact_scales(fmt):
+    """Codes of the correctly rounded quotient for every input: all finite
+    bf16 values under amax values whose scale amax/448 (or amax/6) is inexact,
+    exact, a power of two, below 2^-90 or above 2^125, or subnormal."""
+    rng = np.random.default_rng(31 if fmt == "fp8" else 32)
+    amax = [_bf16_bits(v) for v in (1.0, 3.0, 7.0, 100.0, 0.3, 1e-3, 5e4, 1e-20, 1e30)]
+    amax += [_bf16_bits(v) for v in (448.0, 6.0, 448.0 * 2.0 ** -40, 6.0 * 2.0 ** 20, 1e-25)]
+    amax += [int(b) for b in (rng.integers(0x0080, 0x7F7F, size=6))]     # random finite positives
+    amax += [0x0001, 0x0050, 0x0100, 0x7F7F, 0x7F00]                      # tiny scales, huge amax
+    _quant_sweep(fmt, amax)
