@@ -152,6 +152,7 @@ E2E_STREAMS = 2
 
 
 LAUNCH = {"block_num": -1, "warp_num_per_block": 8}
+LAUNCH_MODE = "manual"   # "auto": per-shape rules from the library's tuning files
 
 
 def make_op(wl, device):
@@ -167,8 +168,28 @@ def make_op(wl, device):
         combine_out_dtype=torch.float32 if wl.combine_out_dtype == "fp32" else torch.bfloat16,
         weighted_combine=wl.weighted, standard_moe=wl.standard_moe, combine_impl=COMBINE_IMPL,
         dispatch_impl=DISPATCH_IMPL, block_num=LAUNCH["block_num"],
-        warp_num_per_block=LAUNCH["warp_num_per_block"])
+        warp_num_per_block=LAUNCH["warp_num_per_block"], launch_config_mode=LAUNCH_MODE)
     return EpDispatchCombineOp(cfg, device)
+
+
+def chosen_kernels(step) -> dict:
+    """The dispatch and combine kernels the library ran for this step, from
+    the handle's launch configuration and the library's automatic rules (bulk
+    copies from 8192 source tokens: 2D combine with up to 8 ranks, copy-mode
+    dispatch)."""
+    from combine_route_layout_gb300 import ep as E
+    wl = step.wl
+    dimpl = step.op.get_launch_config(E.EP_PHASE_DISPATCH)[0]
+    cimpl = step.op.get_launch_config(E.EP_PHASE_COMBINE)[0]
+    many = step.Ttot >= 8192
+    cb_ok = (wl.topk if wl.standard_moe else wl.world_size) <= 8
+    cbulk = cb_ok and cimpl != "vector" and (cimpl == "bulk" or (many and not wl.standard_moe))
+    quant = wl.dispatch_dtype in ("fp8", "fp4")
+    dbulk = not quant and dimpl != "vector" and (dimpl == "bulk" or many)
+    return {"combine": "combine_bulk_kernel" if cbulk else
+            ("combine_std_kernel" if wl.standard_moe else "combine_2d_kernel"),
+            "dispatch": "dispatch_quant_kernel" if quant else
+            ("dispatch_bulk_copy_kernel" if dbulk else "dispatch_copy_kernel")}
 
 
 class Step:
@@ -499,6 +520,8 @@ def main():
     ap.add_argument("--workload", default="ds_v3_throughput", choices=sorted(WORKLOADS))
     ap.add_argument("--latency-workload", default="ds_v3_latency")
     ap.add_argument("--combine-impl", default="auto", choices=["auto", "vector", "bulk"])
+    ap.add_argument("--launch-mode", default="manual", choices=["manual", "auto"],
+                    help="auto: launch parameters from the library's tuning files")
     ap.add_argument("--dispatch-impl", default="auto", choices=["auto", "vector", "bulk"])
     ap.add_argument("--sweep", action="store_true",
                     help="time dispatch/combine over launch configurations instead")
@@ -518,9 +541,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    global COMBINE_IMPL, DISPATCH_IMPL, E2E_STREAMS
+    global COMBINE_IMPL, DISPATCH_IMPL, E2E_STREAMS, LAUNCH_MODE
     COMBINE_IMPL = args.combine_impl
     DISPATCH_IMPL = args.dispatch_impl
+    LAUNCH_MODE = args.launch_mode
     E2E_STREAMS = max(1, args.e2e_streams)
     rank, world, local = dist_setup(args.gpus)
     wl = WORKLOADS[args.workload]
@@ -561,14 +585,7 @@ def main():
     dom = "combine" if c_mean >= d_mean else "dispatch"
     dom_key = {"combine": "combine_2d" if not wl.standard_moe else "combine_std",
                "dispatch": "dispatch_2d" if not wl.standard_moe else "dispatch_std"}[dom]
-    # the kernel the library runs for that step (its EP_COMBINE_AUTO rule: bulk copies
-    # for the 2D layout from 8192 source tokens and up to 8 ranks)
-    bulk = (COMBINE_IMPL == "bulk" or (COMBINE_IMPL == "auto" and step.Ttot >= 8192)) \
-        and wl.world_size <= 8 and not wl.standard_moe
-    dom_kernel = {"combine": "combine_bulk_kernel" if bulk else
-                  ("combine_std_kernel" if wl.standard_moe else "combine_2d_kernel"),
-                  "dispatch": "dispatch_quant_kernel" if wl.dispatch_dtype in ("fp8", "fp4")
-                  else "dispatch_copy_kernel"}[dom]
+    dom_kernel = chosen_kernels(step)[dom]
     ach = c_gbs if dom == "combine" else d_gbs
     tr = profiled_traffic(dom_key)
     if tr and not tr["kernel"].startswith(dom_kernel.replace("_kernel", "")):
@@ -584,6 +601,7 @@ def main():
                    "combine_out": wl.combine_out_dtype, "standard_moe": wl.standard_moe,
                    "l2": "inputs larger than L2 (129 MB); no flush",
                    "copies_C": step.C, "packed_rows_P": step.P,
+                   "launch_mode": LAUNCH_MODE, "kernels": chosen_kernels(step),
                    "parallelism": f"replicas x{world}, 8 simulated EP ranks each"},
         "dispatch": {"us_median": round(d_us, 2), "us_mean": round(d_mean, 2),
                      "bytes": b["dispatch"], "GBps": round(d_gbs, 1),

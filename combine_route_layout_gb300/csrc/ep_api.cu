@@ -273,6 +273,7 @@ struct ep_handle {
   bool has2d, hasstd, needs_init;
   int ntok[EP_MAX_WORLD_SIZE];
   int sm_count;
+  int lc_blocks[2], lc_warps[2];  // launch configuration per ep_phase
 };
 
 namespace {
@@ -291,15 +292,12 @@ ep_status ensure_ready_device(ep_handle* h, cudaStream_t st) {
   return EP_OK;
 }
 
-int block_threads(const ep_handle* h) {
-  const int w = h->cfg.warp_num_per_block > 0 ? h->cfg.warp_num_per_block : 8;
-  return w * 32;
-}
-
-ep::LaunchCfg launch_cfg(const ep_handle* h) {
+// Launch configuration of a phase (EP_PHASE_DISPATCH: layout, dispatch and
+// convert_dispatch_output; EP_PHASE_COMBINE: combine and convert_combine_input).
+ep::LaunchCfg launch_cfg(const ep_handle* h, int phase) {
   ep::LaunchCfg lc;
-  lc.grid_hint = h->cfg.block_num;
-  lc.block = block_threads(h);
+  lc.grid_hint = h->lc_blocks[phase];
+  lc.block = (h->lc_warps[phase] > 0 ? h->lc_warps[phase] : 8) * 32;
   lc.sm_count = h->sm_count;
   return lc;
 }
@@ -411,6 +409,10 @@ ep_status ep_config_create(const ep_config* cfg, void* d_workspace, size_t works
     return fail(EP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   ep_handle* h = new ep_handle();
   h->cfg = *cfg;
+  for (int ph = 0; ph < 2; ++ph) {
+    h->lc_blocks[ph] = cfg->block_num;
+    h->lc_warps[ph] = cfg->warp_num_per_block;
+  }
   h->g = g;
   h->ws = static_cast<uint8_t*>(d_workspace);
   h->ws_bytes = workspace_bytes;
@@ -470,8 +472,9 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
   }
   cudaError_t e = ep::launch_layout_2d(lp, st);
   if (e != cudaSuccess) return cuda_fail(e, "routing-layout launch");
-  e = bulk ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h), st)
-           : ep::launch_dispatch_2d(dp, h->g.quant ? h->cfg.quant_type : 0, launch_cfg(h), st);
+  e = bulk ? ep::launch_dispatch_bulk_copy(dp, false, launch_cfg(h, EP_PHASE_DISPATCH), st)
+           : ep::launch_dispatch_2d(dp, h->g.quant ? h->cfg.quant_type : 0,
+                                    launch_cfg(h, EP_PHASE_DISPATCH), st);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
 
   h->state = kDispatched;
@@ -526,9 +529,9 @@ ep_status ep_combine(ep_handle* h, const void* expert_out, const float* weights,
   p.err = h->w.err;
   cudaError_t e = use_bulk(h, p, false)
                       ? ep::launch_combine_2d_bulk(p, h->cfg.combine_dtype,
-                                                   h->cfg.combine_out_dtype, launch_cfg(h), st)
+                                                   h->cfg.combine_out_dtype, launch_cfg(h, EP_PHASE_COMBINE), st)
                       : ep::launch_combine_2d(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
-                                              launch_cfg(h), st);
+                                              launch_cfg(h, EP_PHASE_COMBINE), st);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   h->state = kCombined;
   if (call_reset) return ep_reset(h, stream);
@@ -599,8 +602,9 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
   dp.out_scales = h->w.packed_scales;
   dp.err = h->w.err;
   e = use_bulk_dispatch(h, dp)
-          ? ep::launch_dispatch_bulk_copy(dp, true, launch_cfg(h), st)
-          : ep::launch_dispatch_std(dp, h->g.quant ? h->cfg.quant_type : 0, launch_cfg(h), st);
+          ? ep::launch_dispatch_bulk_copy(dp, true, launch_cfg(h, EP_PHASE_DISPATCH), st)
+          : ep::launch_dispatch_std(dp, h->g.quant ? h->cfg.quant_type : 0,
+                                    launch_cfg(h, EP_PHASE_DISPATCH), st);
   if (e != cudaSuccess) return cuda_fail(e, "standard-MoE dispatch launch");
 
   h->state = kDispatched;
@@ -651,9 +655,9 @@ ep_status ep_combine_standard_moe(ep_handle* h, const void* expert_out, const fl
   p.err = h->w.err;
   cudaError_t e = use_bulk(h, p, true)
                       ? ep::launch_combine_std_bulk(p, h->cfg.combine_dtype,
-                                                    h->cfg.combine_out_dtype, launch_cfg(h), st)
+                                                    h->cfg.combine_out_dtype, launch_cfg(h, EP_PHASE_COMBINE), st)
                       : ep::launch_combine_std(p, h->cfg.combine_dtype, h->cfg.combine_out_dtype,
-                                               launch_cfg(h), st);
+                                               launch_cfg(h, EP_PHASE_COMBINE), st);
   if (e != cudaSuccess) return cuda_fail(e, "standard-MoE combine launch");
   h->state = kCombined;
   if (call_reset) return ep_reset(h, stream);
@@ -707,7 +711,7 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
   // row_map entries of dropped / foreign slots stay -1
   cudaError_t e = cudaMemsetAsync(h->w.row_map, 0xFF, (size_t)g.R * g.Tmax * g.k * 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-  e = ep::launch_convert_dispatch(p, g.scale_row_bytes > 0, launch_cfg(h), st);
+  e = ep::launch_convert_dispatch(p, g.scale_row_bytes > 0, launch_cfg(h, EP_PHASE_DISPATCH), st);
   if (e != cudaSuccess) return cuda_fail(e, "convert_dispatch_output launch");
   h->hasstd = true;
   if (out) {
@@ -750,8 +754,40 @@ ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* com
   p.packed_y = static_cast<const uint8_t*>(packed_y);
   p.combine_in = static_cast<uint8_t*>(combine_in);
   cudaError_t e = ep::launch_convert_combine(p, h->cfg.combine_dtype,
-                                             launch_cfg(h), st);
+                                             launch_cfg(h, EP_PHASE_COMBINE), st);
   if (e != cudaSuccess) return cuda_fail(e, "convert_combine_input launch");
+  return EP_OK;
+}
+
+ep_status ep_set_launch_config(ep_handle* h, int32_t phase, int32_t impl, int32_t block_num,
+                               int32_t warp_num_per_block) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (phase != EP_PHASE_DISPATCH && phase != EP_PHASE_COMBINE)
+    return fail(EP_ERR_INVALID_ARG, "unknown phase %d", phase);
+  if (warp_num_per_block > 8) return fail(EP_ERR_INVALID_ARG, "warp_num_per_block must be <= 8");
+  if (phase == EP_PHASE_DISPATCH) {
+    if (impl < EP_DISPATCH_AUTO || impl > EP_DISPATCH_BULK)
+      return fail(EP_ERR_INVALID_ARG, "unknown dispatch_impl %d", impl);
+    h->cfg.dispatch_impl = impl;
+  } else {
+    if (impl < EP_COMBINE_AUTO || impl > EP_COMBINE_BULK)
+      return fail(EP_ERR_INVALID_ARG, "unknown combine_impl %d", impl);
+    h->cfg.combine_impl = impl;
+  }
+  h->lc_blocks[phase] = block_num;
+  h->lc_warps[phase] = warp_num_per_block;
+  return EP_OK;
+}
+
+ep_status ep_get_launch_config(const ep_handle* h, int32_t phase, int32_t* impl,
+                               int32_t* block_num, int32_t* warp_num_per_block) {
+  if (!h || !impl || !block_num || !warp_num_per_block)
+    return fail(EP_ERR_INVALID_ARG, "NULL argument");
+  if (phase != EP_PHASE_DISPATCH && phase != EP_PHASE_COMBINE)
+    return fail(EP_ERR_INVALID_ARG, "unknown phase %d", phase);
+  *impl = phase == EP_PHASE_DISPATCH ? h->cfg.dispatch_impl : h->cfg.combine_impl;
+  *block_num = h->lc_blocks[phase];
+  *warp_num_per_block = h->lc_warps[phase];
   return EP_OK;
 }
 

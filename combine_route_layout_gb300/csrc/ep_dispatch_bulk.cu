@@ -155,7 +155,12 @@ cudaError_t launch_dispatch_bulk_copy(const DispatchParams& p, bool std_layout,
   auto k = std_layout ? dispatch_bulk_copy_kernel<true> : dispatch_bulk_copy_kernel<false>;
   const size_t smem = 128 + (size_t)kStages * p.in_row_bytes;
   const int per_sm = ctas_per_sm(k, 32, smem);  // also raises the smem limit
-  int64_t grid = lc.grid_hint > 0 ? lc.grid_hint : (int64_t)lc.sm_count * per_sm;
+  // default: one resident wave; for the packed layout, whose tokens carry
+  // very different row counts, several waves (8 CTAs per SM requested) so
+  // CTAs that finish early hand their SM to the next ones (measured on GB300:
+  // 9 % faster for Zipf-skewed routing, 2 % slower for the 2D layout)
+  int64_t grid = lc.grid_hint > 0 ? lc.grid_hint
+                                  : (int64_t)lc.sm_count * (std_layout && per_sm < 8 ? 8 : per_sm);
   if (grid > ntokens) grid = ntokens;
   return launch_pdl(k, (int)grid, 32, smem, st, p);
 }

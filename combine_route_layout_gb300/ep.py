@@ -39,6 +39,13 @@ EP_QUANT_FP4_E2M1_BLOCK32 = 2
 EP_COMBINE_AUTO = 0
 EP_COMBINE_VECTOR = 1
 EP_COMBINE_BULK = 2
+EP_DISPATCH_AUTO = 0
+EP_DISPATCH_VECTOR = 1
+EP_DISPATCH_BULK = 2
+EP_PHASE_DISPATCH = 0
+EP_PHASE_COMBINE = 1
+IMPL_OF = {"auto": 0, "vector": 1, "bulk": 2}        # same codes for both phases
+IMPL_NAME = {v: k for k, v in IMPL_OF.items()}
 
 _FP4X2 = getattr(torch, "float4_e2m1fn_x2", None)   # packed pairs of E2M1 codes
 _TORCH_OF = {EP_DTYPE_BF16: torch.bfloat16, EP_DTYPE_FP32: torch.float32,
@@ -104,6 +111,8 @@ def _load() -> ctypes.CDLL:
         "ep_last_error": (ctypes.c_char_p, []),
         "ep_routing_layout_noalloc": (S, [I, I, I, I, P, P, P, P, P, P, P]),
         "ep_get_registered_combine_input_buffer": (S, [P, P]),
+        "ep_set_launch_config": (S, [P, I, I, I, I]),
+        "ep_get_launch_config": (S, [P, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -206,6 +215,18 @@ def ep_last_error() -> str:
     return _lib.ep_last_error().decode()
 
 
+def ep_set_launch_config(handle, phase: int, impl: int, block_num: int,
+                         warp_num_per_block: int) -> None:
+    _check(_lib.ep_set_launch_config(handle, phase, impl, block_num, warp_num_per_block))
+
+
+def ep_get_launch_config(handle, phase: int) -> tuple[int, int, int]:
+    impl, bn, wp = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.ep_get_launch_config(handle, phase, ctypes.byref(impl), ctypes.byref(bn),
+                                     ctypes.byref(wp)))
+    return impl.value, bn.value, wp.value
+
+
 def ep_routing_layout_noalloc(world_size, max_num_inp_token_per_rank, num_experts_per_rank,
                               num_experts_per_token, indices, num_tokens, recv_num_token,
                               src_token_pos, slot_map, error_flags, stream) -> None:
@@ -243,20 +264,30 @@ class EpDispatchCombineConfig:
     combine_impl: str = "auto"          # "auto" | "vector" | "bulk"
     dispatch_impl: str = "auto"         # "auto" | "vector" | "bulk" (copy mode)
     use_external_inp_buf: bool = True   # False: reserve a registered combine input buffer
+    # "manual": block_num / warp_num_per_block above, or per-call overrides;
+    # "auto": per-shape rules from the tuning files (User Guide, sections 6
+    # and 10); the environment variable EP_LAUNCH_CONFIG_MODE=AUTO selects it too
+    launch_config_mode: str = "manual"
 
     def to_c(self) -> ep_config:
         c = ep_config()
+        c_fields = {n for n, _ in ep_config._fields_}
         for f in fields(self):
+            if f.name not in c_fields:
+                continue
             v = getattr(self, f.name)
             if f.name in ("data_type", "combine_dtype", "combine_out_dtype"):
                 v = _EP_OF[v]
             elif f.name == "quant_type":
                 v = _QUANT_OF[v]
             elif f.name in ("combine_impl", "dispatch_impl"):
-                v = {"auto": EP_COMBINE_AUTO, "vector": EP_COMBINE_VECTOR,
-                     "bulk": EP_COMBINE_BULK}[v]
+                v = IMPL_OF[v]
             setattr(c, f.name, int(v))
         return c
+
+    def auto_launch(self) -> bool:
+        env = os.environ.get("EP_LAUNCH_CONFIG_MODE", "")
+        return self.launch_config_mode == "auto" or env.upper() == "AUTO"
 
 
 def _ptr(t: torch.Tensor | None):
@@ -282,6 +313,12 @@ class EpDispatchCombineOp:
         self._handle = ep_config_create(self.c, self.workspace.data_ptr(), nbytes)
         R, T = config.world_size, config.max_num_inp_token_per_rank
         self.cap = R * T
+        self._default_launch = {
+            EP_PHASE_DISPATCH: (self.c.dispatch_impl, self.c.block_num, self.c.warp_num_per_block),
+            EP_PHASE_COMBINE: (self.c.combine_impl, self.c.block_num, self.c.warp_num_per_block)}
+        self._applied_launch = dict(self._default_launch)
+        self._auto = config.auto_launch()
+        self._rules = {}
 
     def __del__(self):
         h = getattr(self, "_handle", None)
@@ -299,10 +336,13 @@ class EpDispatchCombineOp:
         assert 0 <= off and off + nbytes <= self.workspace.numel()
         return self.workspace[off:off + nbytes].view(dtype).view(*shape)
 
+    _last_num_tokens = None  # token counts of the last dispatch (combine's tuning key)
+
     def _num_tokens(self, num_tokens):
         if num_tokens is None:
             R, T = self.config.world_size, self.config.max_num_inp_token_per_rank
-            return [T] * R
+            num_tokens = [T] * R
+        self._last_num_tokens = num_tokens
         return num_tokens
 
     def _payload(self):
@@ -318,12 +358,59 @@ class EpDispatchCombineOp:
             return cfg.data_type, H // 2, None
         return cfg.data_type, H, None
 
+    # launch configuration (User Guide, sections 6 and 10) ---------------------
+    def set_launch_config(self, phase: int, impl: str | int = "auto", block_num: int = -1,
+                          warp_per_block: int = 8) -> None:
+        """Base launch configuration of one phase for the calls that follow
+        (per-call block_num / warp_per_block still override it for one call;
+        auto mode still replaces it where a tuning rule matches)."""
+        code = IMPL_OF[impl] if isinstance(impl, str) else int(impl)
+        ep_set_launch_config(self._handle, phase, code, int(block_num), int(warp_per_block))
+        self._default_launch[phase] = (code, int(block_num), int(warp_per_block))
+        self._applied_launch[phase] = self._default_launch[phase]
+
+    def get_launch_config(self, phase: int) -> tuple[str, int, int]:
+        impl, bn, wp = ep_get_launch_config(self._handle, phase)
+        return IMPL_NAME[impl], bn, wp
+
+    def _tuning_key(self, phase: int) -> tuple[str, str]:
+        """(kernel family, dtype) of a phase as the tuning files name them."""
+        from .tuning import dispatch_dtype_name, combine_dtype_name
+        kernel = "stdmoe" if self.config.standard_moe else "2d"
+        if phase == EP_PHASE_DISPATCH:
+            return kernel, dispatch_dtype_name(self.config)
+        return kernel, combine_dtype_name(self.config)
+
+    def _launch_for(self, phase: int, num_tokens, block_num, warp_per_block) -> None:
+        want = self._default_launch[phase]
+        if self._auto:  # per-call arguments are ignored in auto mode
+            from . import tuning
+            kernel, dt = self._tuning_key(phase)
+            key = (phase, kernel)
+            if key not in self._rules:
+                self._rules[key] = tuning.load_rules(kernel, self.config.world_size,
+                                                     "dispatch" if phase == EP_PHASE_DISPATCH
+                                                     else "combine")
+            n = max(self._num_tokens(num_tokens)) if num_tokens is not None else \
+                self.config.max_num_inp_token_per_rank
+            rule = tuning.lookup(self._rules[key], dt, self.config.hidden_dim, int(n))
+            if rule is not None:
+                want = (IMPL_OF[rule["impl"]], rule["block_num"], rule["warp_per_block"])
+        elif block_num is not None or warp_per_block is not None:
+            want = (want[0], want[1] if block_num is None else int(block_num),
+                    want[2] if warp_per_block is None else int(warp_per_block))
+        if self._applied_launch[phase] != want:
+            ep_set_launch_config(self._handle, phase, *want)
+            self._applied_launch[phase] = want
+
     @staticmethod
     def decode_send_flat_idx(pos: int, world_size: int, max_tokens: int) -> tuple[int, int]:
         return divmod(int(pos), world_size * max_tokens)
 
     # section 3 ----------------------------------------------------------------
-    def dispatch(self, input, weights, scales, indices, num_tokens=None):
+    def dispatch(self, input, weights, scales, indices, num_tokens=None, block_num=None,
+                 warp_per_block=None):
+        self._launch_for(EP_PHASE_DISPATCH, num_tokens, block_num, warp_per_block)
         o = ep_dispatch(self._handle, _ptr(input), _ptr(weights), _ptr(scales), _ptr(indices),
                         self._num_tokens(num_tokens), _stream())
         # the outputs always live at the same workspace offsets: build the views once
@@ -351,8 +438,9 @@ class EpDispatchCombineOp:
         return x, w, sc, idx, recv
 
     def combine(self, input, weights, indices, out=None, out_weights=None, call_reset=False,
-                want_weights=True):
+                want_weights=True, block_num=None, warp_per_block=None):
         cfg = self.config
+        self._launch_for(EP_PHASE_COMBINE, self._last_num_tokens, block_num, warp_per_block)
         R, T, H, k = (cfg.world_size, cfg.max_num_inp_token_per_rank, cfg.hidden_dim,
                       cfg.num_experts_per_token)
         dev = self.workspace.device
@@ -400,14 +488,18 @@ class EpDispatchCombineOp:
             "rank_rows": self._view(o.rank_rows, torch.int32, (R,)),
         }
 
-    def dispatch_standard_moe(self, input, weights, scales, indices, num_tokens=None):
+    def dispatch_standard_moe(self, input, weights, scales, indices, num_tokens=None,
+                              block_num=None, warp_per_block=None):
+        self._launch_for(EP_PHASE_DISPATCH, num_tokens, block_num, warp_per_block)
         o = ep_dispatch_standard_moe(self._handle, _ptr(input), _ptr(weights), _ptr(scales),
                                      _ptr(indices), self._num_tokens(num_tokens), _stream())
         self.pcap = o.pcap
         return self._std_views(o)
 
-    def combine_standard_moe(self, input, weights, indices, out=None, call_reset=False):
+    def combine_standard_moe(self, input, weights, indices, out=None, call_reset=False,
+                             block_num=None, warp_per_block=None):
         cfg = self.config
+        self._launch_for(EP_PHASE_COMBINE, self._last_num_tokens, block_num, warp_per_block)
         R, T, H = cfg.world_size, cfg.max_num_inp_token_per_rank, cfg.hidden_dim
         if out is None:
             out = torch.empty((R, T, H), dtype=cfg.combine_out_dtype, device=input.device)

@@ -80,6 +80,14 @@ typedef enum {
                                    always uses the vector kernel */
 } ep_dispatch_impl;
 
+/* The two phases whose launch configuration can be set separately
+ * (ep_set_launch_config). */
+typedef enum {
+    EP_PHASE_DISPATCH = 0,      /* routing layout, dispatch, dispatch_standard_moe,
+                                   convert_dispatch_output */
+    EP_PHASE_COMBINE = 1        /* combine, combine_standard_moe, convert_combine_input */
+} ep_phase;
+
 typedef enum {
     EP_QUANT_NONE = 0,          /* dispatch moves the input bits unchanged */
     EP_QUANT_FP8_E4M3_BLOCK128 = 1, /* bf16 in; E4M3 codes + one f32 scale per 128 elements out */
@@ -279,6 +287,24 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
  */
 ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* combine_in,
                                    void* stream);
+
+/*
+ * Launch configuration of one phase (ep_phase) for the calls that follow:
+ * `impl` is an ep_dispatch_impl (EP_PHASE_DISPATCH) or ep_combine_impl
+ * (EP_PHASE_COMBINE); block_num and warp_num_per_block as in ep_config
+ * (<= 0: automatic; at most 8 warps). The User Guide, section 6 (Launch
+ * Configuration) lets each call override block_num / warp_per_block, and
+ * section 10 (Tuning) reads per-shape launch parameters from tuning files
+ * at run time; a binding does both through this setter. Results do not
+ * depend on the launch configuration. Host only; any state. Errors:
+ * EP_ERR_INVALID_ARG for an unknown phase or impl or more than 8 warps.
+ */
+ep_status ep_set_launch_config(ep_handle* h, int32_t phase, int32_t impl, int32_t block_num,
+                               int32_t warp_num_per_block);
+
+/* The phase's current launch configuration (as set above, or from ep_config). */
+ep_status ep_get_launch_config(const ep_handle* h, int32_t phase, int32_t* impl,
+                               int32_t* block_num, int32_t* warp_num_per_block);
 
 /*
  * (+) Wait for `stream`, then report and clear device-detected errors

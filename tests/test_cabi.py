@@ -151,3 +151,25 @@ def test_state_machine_without_device(ep):
         assert "registered" in ep.ep_last_error()
     finally:
         ep.ep_destroy(h)
+
+
+def test_launch_config_per_phase(ep):
+    """ep_set_launch_config / ep_get_launch_config: per phase, validated,
+    starting from the config's block_num / warp_num_per_block."""
+    c = small(ep, block_num=300, warp_num_per_block=4)
+    h = ep.ep_config_create(c, FAKE, ep.ep_workspace_size(c))
+    try:
+        assert ep.ep_get_launch_config(h, ep.EP_PHASE_DISPATCH) == (0, 300, 4)
+        assert ep.ep_get_launch_config(h, ep.EP_PHASE_COMBINE) == (0, 300, 4)
+        ep.ep_set_launch_config(h, ep.EP_PHASE_COMBINE, ep.EP_COMBINE_BULK, 456, 8)
+        assert ep.ep_get_launch_config(h, ep.EP_PHASE_COMBINE) == (2, 456, 8)
+        assert ep.ep_get_launch_config(h, ep.EP_PHASE_DISPATCH) == (0, 300, 4)
+        ep.ep_set_launch_config(h, ep.EP_PHASE_DISPATCH, ep.EP_DISPATCH_VECTOR, -1, 2)
+        assert ep.ep_get_launch_config(h, ep.EP_PHASE_DISPATCH) == (1, -1, 2)
+        for bad in [(2, 0, -1, 8), (0, 3, -1, 8), (1, -1, -1, 8), (0, 0, -1, 9)]:
+            with pytest.raises(ep.EpError) as ei:
+                ep.ep_set_launch_config(h, *bad)
+            assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        assert ep.ep_get_launch_config(h, ep.EP_PHASE_DISPATCH) == (1, -1, 2)
+    finally:
+        ep.ep_destroy(h)

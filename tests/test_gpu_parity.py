@@ -5,6 +5,8 @@ benchmark tables; the small variants keep several 256-token chunks and a
 ragged tail so every tile path runs. Full-size cases compare all routing
 metadata exactly and payload / combine rows on a seeded sample.
 """
+import json
+
 import numpy as np
 import pytest
 import torch
@@ -957,3 +959,79 @@ def test_quant_codes_every_bf16_value_inexact_scales(fmt):
     amax += [int(b) for b in (rng.integers(0x0080, 0x7F7F, size=6))]     # random finite positives
     amax += [0x0001, 0x0050, 0x0100, 0x7F7F, 0x7F00]                      # tiny scales, huge amax
     _quant_sweep(fmt, amax)
+
+
+# ---------------------------------------- launch configuration and tuning files
+
+def test_launch_config_per_call_and_auto_mode(tmp_path, monkeypatch):
+    """Per-call block_num / warp_per_block (User Guide, section 6) and auto
+    mode reading per-shape rules from a tuning file (section 10): the handle
+    takes the chosen launch configuration per phase, and results stay bit
+    for bit those of the default configuration."""
+    from combine_route_layout_gb300 import tuning
+    wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=300, hidden=1024)
+    inp = Inputs(wl, 5, ragged=True)
+    y = make_expert_outputs(wl, wl.world_size * wl.tokens_per_rank, 5, device=DEV)
+    ref_op = EpDispatchCombineOp(make_config(wl))
+    rd = ref_op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    ref_x, ref_sc = rd[0].clone(), rd[2].clone()
+    ref_out, _ = ref_op.combine(y, rd[1], None, call_reset=True)
+
+    d = str(tmp_path)
+    monkeypatch.setenv("EP_TUNING_CONFIG_DIR", d)
+    tuning.save_rule("2d", 8, "dispatch", {"dtype": "fp8", "num_tokens": 512, "hidden_dim": 1024,
+                                           "impl": "vector", "block_num": 152,
+                                           "warp_per_block": 4}, d)
+    tuning.save_rule("2d", 8, "combine", {"dtype": "bf16", "num_tokens": 512, "hidden_dim": 1024,
+                                          "impl": "bulk", "block_num": 304,
+                                          "warp_per_block": 8}, d)
+    op = EpDispatchCombineOp(make_config(wl, launch_config_mode="auto"))
+    dd = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    assert op.get_launch_config(E.EP_PHASE_DISPATCH) == ("vector", 152, 4)
+    out, _ = op.combine(y, dd[1], None, call_reset=True)
+    assert op.get_launch_config(E.EP_PHASE_COMBINE) == ("bulk", 304, 8)
+    op.sync()
+    recv = host(rd[4])
+    for r in range(wl.world_size):
+        n = recv[r]
+        assert np.array_equal(host(dd[0])[r, :n], host(ref_x)[r, :n])
+        assert np.array_equal(host(dd[2])[r, :n].view(np.uint32), host(ref_sc)[r, :n].view(np.uint32))
+    def same_valid(a, b):   # rows past a rank's token count are never written
+        ga, gb = host(a), host(b)
+        return all(np.array_equal(ga[s, :n], gb[s, :n]) for s, n in enumerate(inp.ntok))
+
+    assert same_valid(out, ref_out)
+
+    man = EpDispatchCombineOp(make_config(wl))
+    md = man.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok, block_num=456, warp_per_block=2)
+    assert man.get_launch_config(E.EP_PHASE_DISPATCH) == ("auto", 456, 2)
+    mout, _ = man.combine(y, md[1], None, call_reset=True, block_num=76, warp_per_block=4)
+    assert man.get_launch_config(E.EP_PHASE_COMBINE) == ("auto", 76, 4)
+    assert same_valid(mout, ref_out)
+    md = man.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)   # back to the config's
+    assert man.get_launch_config(E.EP_PHASE_DISPATCH) == ("auto", -1, 8)
+    man.reset()
+    man.set_launch_config(E.EP_PHASE_DISPATCH, "vector", 304, 4)     # a new base setting
+    md = man.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    assert man.get_launch_config(E.EP_PHASE_DISPATCH) == ("vector", 304, 4)
+    man.reset()
+
+
+@pytest.mark.parametrize("std", [False, True])
+def test_tuner_sweeps_and_writes_rules(tmp_path, monkeypatch, std):
+    """The tuner times its candidates on a small shape and saves the fastest."""
+    from combine_route_layout_gb300 import tuning
+    monkeypatch.setitem(tuning.SCOPES, "tiny", {"grids": [-1, 152], "warps": [8],
+                                                "bulk_grids": [-1]})
+    wl = WORKLOADS["skewed_zipf_std_moe" if std else "ds_v3_latency"].with_(
+        tokens_per_rank=64, hidden=512)
+    cfg = make_config(wl)
+    for phase in ("dispatch", "combine"):
+        rule = tuning.tune_shape(cfg, phase, "tiny", iters=3)
+        assert rule["num_tokens"] == 64 and rule["hidden_dim"] == 512
+        assert rule["impl"] in ("vector", "bulk") and rule["latency_us"] > 0
+        assert rule["candidates"] == len(tuning._candidates(phase, cfg, "tiny")) >= 2
+        p = tuning.save_rule("stdmoe" if std else "2d", 8, phase, rule, str(tmp_path))
+        assert tuning.lookup(tuning.load_rules("stdmoe" if std else "2d", 8, phase,
+                                               str(tmp_path)),
+                             rule["dtype"], 512, 64) == json.load(open(p))["rules"][0]
