@@ -303,7 +303,10 @@ class EpDispatchCombineOp:
     ranks: x [R, Tmax, H], weights [R, Tmax, k], indices [R, Tmax, k] int32;
     num_tokens gives each source rank's token count (default Tmax)."""
 
-    def __init__(self, config: EpDispatchCombineConfig, device: torch.device | str = "cuda"):
+    def __init__(self, config: EpDispatchCombineConfig, device: torch.device | str = "cuda",
+                 use_tuning_files: bool | None = None):
+        """use_tuning_files: None follows config.launch_config_mode and the
+        EP_LAUNCH_CONFIG_MODE environment variable; False or True overrides both."""
         self.config = config
         self.c = config.to_c()
         nbytes = ep_workspace_size(self.c)
@@ -317,8 +320,9 @@ class EpDispatchCombineOp:
             EP_PHASE_DISPATCH: (self.c.dispatch_impl, self.c.block_num, self.c.warp_num_per_block),
             EP_PHASE_COMBINE: (self.c.combine_impl, self.c.block_num, self.c.warp_num_per_block)}
         self._applied_launch = dict(self._default_launch)
-        self._auto = config.auto_launch()
+        self._auto = config.auto_launch() if use_tuning_files is None else bool(use_tuning_files)
         self._rules = {}
+        self._rule_choice = {}
 
     def __del__(self):
         h = getattr(self, "_handle", None)
@@ -391,11 +395,14 @@ class EpDispatchCombineOp:
                 self._rules[key] = tuning.load_rules(kernel, self.config.world_size,
                                                      "dispatch" if phase == EP_PHASE_DISPATCH
                                                      else "combine")
-            n = max(self._num_tokens(num_tokens)) if num_tokens is not None else \
+            n = int(max(num_tokens)) if num_tokens is not None else \
                 self.config.max_num_inp_token_per_rank
-            rule = tuning.lookup(self._rules[key], dt, self.config.hidden_dim, int(n))
-            if rule is not None:
-                want = (IMPL_OF[rule["impl"]], rule["block_num"], rule["warp_per_block"])
+            if (phase, n) not in self._rule_choice:
+                rule = tuning.lookup(self._rules[key], dt, self.config.hidden_dim, n)
+                self._rule_choice[(phase, n)] = None if rule is None else (
+                    IMPL_OF[rule["impl"]], rule["block_num"], rule["warp_per_block"])
+            if self._rule_choice[(phase, n)] is not None:
+                want = self._rule_choice[(phase, n)]
         elif block_num is not None or warp_per_block is not None:
             want = (want[0], want[1] if block_num is None else int(block_num),
                     want[2] if warp_per_block is None else int(warp_per_block))

@@ -139,8 +139,7 @@ def tune_shape(cfg, phase: str, scope: str = "quick", iters: int = 20, seed: int
     idx = idx.to(torch.int32).reshape(R, T, k).contiguous()
     w = torch.softmax(torch.randn((R, T, k), generator=g, device=dev), dim=-1)
     x = torch.randn((R, T, H), generator=g, device=dev).to(cfg.data_type)
-    op = EpDispatchCombineOp(cfg)
-    op._auto = False  # the candidates below, not the tuning files, set the launch
+    op = EpDispatchCombineOp(cfg, use_tuning_files=False)  # the candidates set the launch
     ph = EP_PHASE_DISPATCH if phase == "dispatch" else EP_PHASE_COMBINE
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
