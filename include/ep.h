@@ -51,7 +51,7 @@ typedef enum {
     EP_ERR_CUDA = -5,           /* a CUDA runtime call failed; see ep_last_error() */
     EP_ERR_TIMEOUT = -6,        /* a kernel's bounded wait gave up (reported by ep_sync) */
     EP_ERR_WORKSPACE = -7,      /* workspace NULL, misaligned or too small */
-    EP_ERR_UNSUPPORTED = -8     /* valid request this build does not implement */
+    EP_ERR_UNSUPPORTED = -8     /* valid request the library does not implement */
 } ep_status;
 
 typedef enum {
