@@ -206,23 +206,33 @@ __device__ __forceinline__ void quant16(const uint4& a, const uint4& b, uint4& q
   q.w = c[6] | (c[7] << 16);
 }
 
-// FP4: the same 16 elements per lane, now half of a 32-element block; the
-// block's amax is reduced over the lane pair, scale = amax / 6.
-__device__ __forceinline__ void quant16_fp4(const uint4& a, const uint4& b, uint2& q,
-                                            float& scale) {
-  float f[16];
-  unpack16(a, b, f);
+// FP4 with a whole 32-element block per lane (32 consecutive elements, four
+// 16-byte loads): the block's amax needs no shuffle, and each destination row
+// takes one 16-byte store of codes and one 4-byte scale store per lane.
+__device__ __forceinline__ void quant32_fp4(const uint4 v[4], uint4& q, float& scale) {
+  const uint32_t w[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                          v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  for (int i = 0; i < 16; ++i)
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
   scale = __fdiv_rn(amax, 6.0f);
-  if (amax != 0.f) {
+  uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], scale);
+  for (int h = 0; h < 4; ++h) {
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = bf16_lo(w[4 * h + j]);
+      f[2 * j + 1] = bf16_hi(w[4 * h + j]);
+    }
+    if (amax != 0.f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = __fdiv_rn(f[j], scale);
+    }
+    out[h] = cvt_e2m1x8(f);
   }
-  q.x = cvt_e2m1x8(f);
-  q.y = cvt_e2m1x8(f + 8);
+  q = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 template <bool STD, bool FP4>
@@ -239,25 +249,31 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
     if (t >= p.ntok[s]) continue;
 
     const uint8_t* src = p.x + g * p.in_row_bytes;
-    uint4 a[kQuantUnroll], b[kQuantUnroll];
-#pragma unroll
-    for (int i = 0; i < kQuantUnroll; ++i) {
-      const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
-      if (e0 < p.H) {
-        a[i] = ld_nc_v4(src + (int64_t)e0 * 2);
-        b[i] = ld_nc_v4(src + (int64_t)e0 * 2 + 16);
-      } else {
-        a[i] = make_uint4(0, 0, 0, 0);
-        b[i] = a[i];
-      }
-    }
     uint4 q[kQuantUnroll];
-    uint2 q4[kQuantUnroll];
     float sc[kQuantUnroll];
+    // FP4: lane covers elements e32 .. e32 + 31 of the unit's 1024
+    const int e32 = seg * (kQuantUnroll * 512) + lane * 32;
+    if (FP4) {
+      uint4 v[4];
 #pragma unroll
-    for (int i = 0; i < kQuantUnroll; ++i) {
-      if (FP4) quant16_fp4(a[i], b[i], q4[i], sc[i]);
-      else quant16(a[i], b[i], q[i], sc[i]);
+      for (int i = 0; i < 4; ++i)
+        v[i] = e32 < p.H ? ld_nc_v4(src + (int64_t)e32 * 2 + 16 * i) : make_uint4(0, 0, 0, 0);
+      quant32_fp4(v, q[0], sc[0]);
+    } else {
+      uint4 a[kQuantUnroll], b[kQuantUnroll];
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) {
+        const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
+        if (e0 < p.H) {
+          a[i] = ld_nc_v4(src + (int64_t)e0 * 2);
+          b[i] = ld_nc_v4(src + (int64_t)e0 * 2 + 16);
+        } else {
+          a[i] = make_uint4(0, 0, 0, 0);
+          b[i] = a[i];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kQuantUnroll; ++i) quant16(a[i], b[i], q[i], sc[i]);
     }
     if (!waited) {  // the routing layout is complete and visible past this point
       pdl_wait();
@@ -268,14 +284,16 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
     auto put = [&](int64_t row) {
       uint8_t* dst = p.out_x + row * p.out_row_bytes;
       float* dsc = reinterpret_cast<float*>(p.out_scales) + row * nb;
+      if (FP4) {
+        if (e32 < p.H) {
+          st_v4(dst + e32 / 2, q[0]);
+          dsc[e32 / 32] = sc[0];
+        }
+      } else {
 #pragma unroll
-      for (int i = 0; i < kQuantUnroll; ++i) {
-        const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
-        if (e0 < p.H) {
-          if (FP4) {
-            st_v2(dst + e0 / 2, q4[i]);
-            if ((lane & 1) == 0) dsc[e0 / 32] = sc[i];
-          } else {
+        for (int i = 0; i < kQuantUnroll; ++i) {
+          const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
+          if (e0 < p.H) {
             st_v4(dst + e0, q[i]);
             if ((lane & 7) == 0) dsc[e0 / 128] = sc[i];
           }
