@@ -274,6 +274,12 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
       }
 #pragma unroll
       for (int i = 0; i < kQuantUnroll; ++i) quant16(a[i], b[i], q[i], sc[i]);
+      // the unit's 8 block scales sit in lanes 0, 8, 16, 24 (two each): move
+      // scale j to lane j so each destination takes them in one store
+      static_assert(kQuantUnroll == 2, "scale gather assumes two 512-element steps");
+      const int from = (lane & 3) * 8;
+      const float s0 = __shfl_sync(kFull, sc[0], from), s1 = __shfl_sync(kFull, sc[1], from);
+      sc[0] = lane < 4 ? s0 : s1;
     }
     if (!waited) {  // the routing layout is complete and visible past this point
       pdl_wait();
@@ -293,11 +299,10 @@ __global__ void __launch_bounds__(256, 4) dispatch_quant_kernel(DispatchParams p
 #pragma unroll
         for (int i = 0; i < kQuantUnroll; ++i) {
           const int e0 = (seg * kQuantUnroll + i) * 512 + lane * 16;
-          if (e0 < p.H) {
-            st_v4(dst + e0, q[i]);
-            if ((lane & 7) == 0) dsc[e0 / 128] = sc[i];
-          }
+          if (e0 < p.H) st_v4(dst + e0, q[i]);
         }
+        const int blk = seg * (kQuantUnroll * 4) + lane;  // lanes 0..7: the unit's blocks
+        if (lane < kQuantUnroll * 4 && blk * 128 < p.H) dsc[blk] = sc[0];
       }
     };
     if (!STD) {

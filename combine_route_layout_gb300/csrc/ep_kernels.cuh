@@ -278,10 +278,6 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float f[8]) {
   return r;
 }
 
-__device__ __forceinline__ void st_v2(void* p, uint2 v) {
-  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-
 // Two f32 -> two bf16 (round to nearest even); lo in bits 0..15.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   uint32_t r;
