@@ -791,6 +791,16 @@ ep_status ep_get_launch_config(const ep_handle* h, int32_t phase, int32_t* impl,
   return EP_OK;
 }
 
+ep_status ep_selftest_bounded_wait(ep_handle* h, void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = ensure_ready_device(h, st);
+  if (s != EP_OK) return s;
+  cudaError_t e = ep::launch_bounded_wait_selftest(h->w.err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return EP_OK;
+}
+
 ep_status ep_sync(ep_handle* h, void* stream) {
   if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

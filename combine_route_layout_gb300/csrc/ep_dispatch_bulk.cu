@@ -142,7 +142,25 @@ __global__ void __launch_bounds__(32) dispatch_bulk_copy_kernel(DispatchParams p
   }
 }
 
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// ever completes. The bounded wait gives up after about a second and the
+// kernel records the timeout bit, as every bulk kernel does, then returns
+// normally (no trap, no fault; the context stays usable).
+__global__ void bounded_wait_selftest_kernel(int32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+    if (!mbar_wait(&bar, 0)) atomicOr(err, kErrTimeout);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(int32_t* err, cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(err);
+  return cudaGetLastError();
+}
 
 bool dispatch_bulk_supported(const DispatchParams& p) {
   return p.in_row_bytes <= 48 * 1024 && p.in_row_bytes % 16 == 0;

@@ -188,6 +188,10 @@ cudaError_t launch_combine_2d_bulk(const CombineParams& p, int in_dtype, int out
                                    const LaunchCfg& lc, cudaStream_t st);
 cudaError_t launch_combine_std_bulk(const CombineParams& p, int in_dtype, int out_dtype,
                                     const LaunchCfg& lc, cudaStream_t st);
+// One kernel whose bounded mbarrier wait times out (about 1 s) and sets
+// kErrTimeout in *err.
+cudaError_t launch_bounded_wait_selftest(int32_t* err, cudaStream_t st);
+
 // Copy-mode dispatch with bulk copies (TMA); same results as the vector
 // kernel. Needs source rows of at most 48 KB.
 bool dispatch_bulk_supported(const DispatchParams& p);

@@ -113,6 +113,7 @@ def _load() -> ctypes.CDLL:
         "ep_get_registered_combine_input_buffer": (S, [P, P]),
         "ep_set_launch_config": (S, [P, I, I, I, I]),
         "ep_get_launch_config": (S, [P, I, P, P, P]),
+        "ep_selftest_bounded_wait": (S, [P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -205,6 +206,10 @@ def ep_convert_dispatch_output(handle, dispatch_x, dispatch_indices, stream) -> 
 
 def ep_convert_combine_input(handle, packed_y, combine_in, stream) -> None:
     _check(_lib.ep_convert_combine_input(handle, packed_y, combine_in, stream))
+
+
+def ep_selftest_bounded_wait(handle, stream) -> None:
+    _check(_lib.ep_selftest_bounded_wait(handle, stream))
 
 
 def ep_sync(handle, stream) -> None:

@@ -307,6 +307,15 @@ ep_status ep_get_launch_config(const ep_handle* h, int32_t phase, int32_t* impl,
                                int32_t* block_num, int32_t* warp_num_per_block);
 
 /*
+ * (+) Self-test of failure detection: launches one kernel that waits on a
+ * barrier nothing completes. Its bounded wait gives up after about one
+ * second, sets the handle's timeout flag and returns normally (no trap or
+ * fault), so the next ep_sync reports EP_ERR_TIMEOUT exactly as for a bulk
+ * kernel whose copies never arrived, and the handle stays usable. Async.
+ */
+ep_status ep_selftest_bounded_wait(ep_handle* h, void* stream);
+
+/*
  * (+) Wait for `stream`, then report and clear device-detected errors
  * (EP_ERR_INVALID_INDEX, EP_ERR_CAPACITY) raised by earlier launches.
  */

@@ -377,6 +377,29 @@ def test_invalid_index_sets_error_flag():
     op.reset()
 
 
+def test_bounded_wait_timeout_is_reported_and_the_handle_stays_usable():
+    """Failure detection without a GPU fault: a kernel waits on a barrier that
+    nothing completes; its bounded wait gives up after about a second and
+    sets the timeout flag, ep_sync reports EP_ERR_TIMEOUT once, and the same
+    handle then dispatches correctly."""
+    wl = WORKLOADS["tiny"]
+    inp = Inputs(wl, 0)
+    op = EpDispatchCombineOp(make_config(wl))
+    E.ep_selftest_bounded_wait(op._handle, torch.cuda.current_stream().cuda_stream)
+    with pytest.raises(EpError) as ei:
+        op.sync()
+    assert ei.value.status == E.EP_ERR_TIMEOUT
+    op.sync()                               # flag cleared
+    d_x, _, _, _, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
+    op.sync()
+    recv, src_pos, slot = check_route(inp, recv_d, op.get_dispatch_src_token_pos())
+    x_ref = oracle.place_rows(inp.x_bits(), inp.ntok, slot)
+    gx = host(d_x)
+    for r in range(wl.world_size):
+        assert np.array_equal(gx[r, :recv[r]], x_ref[r, :recv[r]])
+    op.reset()
+
+
 def test_std_capacity_overflow_flagged():
     wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=100, hidden=256)
     inp = Inputs(wl, 0)
