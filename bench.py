@@ -334,11 +334,17 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
 
     # The expert-output rows do not depend on dispatch: they travel on side
     # streams (other copy engines) while the tokens are copied and dispatched.
+    # The output's device->host copy runs on its own stream, so it overlaps
+    # the next step's host->device copies (the link is full duplex); each
+    # step still moves all of its inputs up and its result down.
     side = [torch.cuda.Stream() for _ in range(E2E_STREAMS)]
+    down = torch.cuda.Stream()
+    state = {"combined": None, "read": None}
 
     def one():
-        for sd in side:
-            sd.wait_stream(st)                  # previous combine has read y
+        for sd in side:                           # the previous combine has read y
+            if state["combined"] is not None:
+                sd.wait_event(state["combined"])
         for j, (hsrc, ddst) in enumerate(ycopy):
             with torch.cuda.stream(side[j % len(side)]):
                 ddst.copy_(hsrc, non_blocking=True)
@@ -348,8 +354,16 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
         d = step.dispatch(xd, wd, idd)
         for sd in side:
             st.wait_stream(sd)
+        if state["read"] is not None:             # the previous output has been read
+            st.wait_event(state["read"])
         step.combine(d, w=wd)
-        oh.copy_(step.out, non_blocking=True)
+        state["combined"] = torch.cuda.Event()
+        state["combined"].record(st)
+        down.wait_event(state["combined"])
+        with torch.cuda.stream(down):
+            oh.copy_(step.out, non_blocking=True)
+        state["read"] = torch.cuda.Event()
+        state["read"].record(down)
 
     for _ in range(max(1, W)):
         one()
@@ -360,6 +374,7 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
     t0.record(st)
     for _ in range(K):
         one()
+    st.wait_stream(down)                          # the last output is on the host
     t1.record(st)
     torch.cuda.synchronize()
     dist_barrier()
