@@ -317,63 +317,74 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
     ih = step.idx.cpu().pin_memory()
     # only the expert-output rows the combine reads travel
     used = step.rank_rows if wl.standard_moe else step.recv
-    ycopy, ybytes = [], 0
+    yh, ybytes = [], 0
     for r in range(wl.world_size):
         n = int(used[r])
         if n == 0:
             continue
         h = step.y[r, :n].cpu().pin_memory()
-        ycopy.append((h, step.y[r, :n]))
+        yh.append((r, n, h))
         ybytes += h.numel() * h.element_size()
     oh = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    xd = torch.empty_like(step.x)
-    wd = torch.empty_like(step.w)
-    idd = torch.empty_like(step.idx)
+    # two device copies of every input: step i uploads into set i % 2 while
+    # step i - 1 still computes on the other
+    bufs = [{"x": torch.empty_like(step.x), "w": torch.empty_like(step.w),
+             "idx": torch.empty_like(step.idx), "y": torch.empty_like(step.y)}
+            for _ in range(2)]
     h2d = xh.numel() * xh.element_size() + wh.numel() * 4 + ih.numel() * 4 + ybytes
     d2h = oh.numel() * oh.element_size()
 
-    # The expert-output rows do not depend on dispatch: they travel on side
-    # streams (other copy engines) while the tokens are copied and dispatched.
-    # The output's device->host copy runs on its own stream, so it overlaps
-    # the next step's host->device copies (the link is full duplex); each
-    # step still moves all of its inputs up and its result down.
-    side = [torch.cuda.Stream() for _ in range(E2E_STREAMS)]
+    # Uploads run on their own streams (copy engines) and overlap the
+    # previous step's dispatch and combine; the output's device->host copy
+    # runs on another and overlaps the next uploads (the link is full
+    # duplex). Each step still moves all of its inputs up and its result down.
+    up = [torch.cuda.Stream() for _ in range(E2E_STREAMS)]
     down = torch.cuda.Stream()
-    state = {"combined": None, "read": None}
+    done = [None, None]      # combine of the last step that used each input set
+    state = {"read": None, "i": 0}
 
     def one():
-        for sd in side:                           # the previous combine has read y
-            if state["combined"] is not None:
-                sd.wait_event(state["combined"])
-        for j, (hsrc, ddst) in enumerate(ycopy):
-            with torch.cuda.stream(side[j % len(side)]):
-                ddst.copy_(hsrc, non_blocking=True)
-        xd.copy_(xh, non_blocking=True)
-        wd.copy_(wh, non_blocking=True)
-        idd.copy_(ih, non_blocking=True)
-        d = step.dispatch(xd, wd, idd)
-        for sd in side:
-            st.wait_stream(sd)
+        b = state["i"] % 2
+        state["i"] += 1
+        B = bufs[b]
+        for us in up:
+            if done[b] is not None:
+                us.wait_event(done[b])
+        with torch.cuda.stream(up[0]):
+            B["x"].copy_(xh, non_blocking=True)
+            B["w"].copy_(wh, non_blocking=True)
+            B["idx"].copy_(ih, non_blocking=True)
+        for j, (r, n, h) in enumerate(yh):
+            with torch.cuda.stream(up[(j + 1) % len(up)]):
+                B["y"][r, :n].copy_(h, non_blocking=True)
+        st.wait_stream(up[0])
+        d = step.dispatch(B["x"], B["w"], B["idx"])
+        for us in up[1:]:
+            st.wait_stream(us)
         if state["read"] is not None:             # the previous output has been read
             st.wait_event(state["read"])
-        step.combine(d, w=wd)
-        state["combined"] = torch.cuda.Event()
-        state["combined"].record(st)
-        down.wait_event(state["combined"])
+        step.combine(d, y=B["y"], w=B["w"])
+        done[b] = torch.cuda.Event()
+        done[b].record(st)
+        down.wait_event(done[b])
         with torch.cuda.stream(down):
             oh.copy_(step.out, non_blocking=True)
         state["read"] = torch.cuda.Event()
         state["read"].record(down)
 
-    for _ in range(max(1, W)):
+    for _ in range(max(2, W)):
         one()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     dist_barrier()
     t0.record(st)
+    for us in up + [down]:                        # nothing timed starts before t0
+        us.wait_event(t0)
     for _ in range(K):
         one()
+    for us in up:
+        st.wait_stream(us)
     st.wait_stream(down)                          # the last output is on the host
     t1.record(st)
     torch.cuda.synchronize()
