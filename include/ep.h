@@ -76,8 +76,8 @@ typedef enum {
                                    otherwise */
     EP_DISPATCH_VECTOR = 1,     /* 16-byte vector loads and stores */
     EP_DISPATCH_BULK = 2        /* copy mode only: bulk async copies (TMA) through a
-                                   shared-memory ring, rows <= 48 KB; FP8 quantisation
-                                   always uses the vector kernel */
+                                   shared-memory ring, rows <= 48 KB; quantisation always
+                                   uses the vector kernel */
 } ep_dispatch_impl;
 
 /* The two phases whose launch configuration can be set separately
@@ -138,7 +138,8 @@ typedef struct ep_handle ep_handle;
  * recv_num_token[r] rows of rank r are written.
  */
 typedef struct ep_dispatch_out {
-    void* x;                    /* [R][cap][H] payload: input dtype, or E4M3 codes */
+    void* x;                    /* [R][cap][x_row_bytes] payload: input dtype, E4M3 codes,
+                                   or E2M1 codes two per byte */
     void* scales;               /* [R][cap][scale_row_bytes]; NULL when there are none */
     float* weights;             /* [R][cap][k] router weights of the received token */
     int32_t* indices;           /* [R][cap][k] global expert ids of the token (-1 kept) */
@@ -157,7 +158,8 @@ typedef struct ep_dispatch_out {
  */
 typedef struct ep_std_moe_out {
     void* packed_x;                 /* [R][pcap][H] payload */
-    void* packed_scales;            /* [R][pcap][H/128] f32 with FP8 quantisation, else NULL */
+    void* packed_scales;            /* [R][pcap][H/128] (FP8) or [R][pcap][H/32] (FP4) f32
+                                       with quantisation, else NULL */
     int32_t* packed_count;          /* [R][E_r] rows per local expert */
     int32_t* packed_src_info;       /* [R][pcap] src_token_pos encoding; -1 on padding rows */
     int64_t* packed_layout_range;   /* [R][E_r][R] (begin << 32) | count per source rank,
@@ -190,7 +192,7 @@ void ep_destroy(ep_handle* h);
  *   x          device [R][Tmax][H], data_type; 16-byte aligned
  *   weights    device [R][Tmax][k] f32
  *   scales     device [R][Tmax][scale_dim * scale_type_size bytes] or NULL
- *              (must be NULL with FP8 block quantisation, which computes them)
+ *              (must be NULL with block quantisation, which computes them)
  *   indices    device [R][Tmax][k] int32 in [-1, R*E_r)
  *   num_tokens host [R], tokens held by each source rank, each <= Tmax
  * Receive rows are ordered by (source rank, source token). State must be
