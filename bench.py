@@ -471,6 +471,68 @@ def sweep(wl, dev, K: int, W: int):
             "best_combine": best_c}
 
 
+def convert_leg(wl, dev, K: int, W: int):
+    """The standard-MoE layout reached through the 2D path and the two
+    conversions (User Guide, section 4): dispatch, convert_dispatch_output,
+    convert_combine_input, combine, each timed with CUDA events (inputs
+    larger than L2). Algorithmic bytes: convert_dispatch_output reads each
+    receive row once and writes one packed row plus its src_info per valid
+    (token, slot); convert_combine_input reads every packed row and writes
+    one receive row per (token, destination)."""
+    from combine_route_layout_gb300 import EpDispatchCombineConfig, EpDispatchCombineOp
+    from gen import make_indices, make_num_tokens, make_tokens, make_weights
+    R, T, H, k = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.topk
+    cfg = EpDispatchCombineConfig(
+        data_type=torch.bfloat16, world_size=R, hidden_dim=H, scale_dim=0, scale_type_size=4,
+        max_token_type_size=4, max_num_inp_token_per_rank=T,
+        num_experts_per_rank=wl.experts_per_rank, num_experts_per_token=k,
+        combine_dtype=torch.bfloat16, combine_out_dtype=torch.float32, standard_moe=True)
+    op = EpDispatchCombineOp(cfg, dev)
+    x = make_tokens(wl, device=dev)
+    w = torch.from_numpy(make_weights(wl)).to(dev)
+    idx = torch.from_numpy(make_indices(wl)).to(dev)
+    ntok = make_num_tokens(wl)
+    st = torch.cuda.current_stream()
+    d = op.dispatch(x, w, None, idx, ntok)
+    px, pcount, psrc, prange = op.convert_dispatch_output(d[0], d[3])
+    torch.cuda.synchronize()
+    C = int(d[4].sum())
+    P = int((idx >= 0).sum())
+    y = torch.randn(px.shape, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    y2d = op.convert_combine_input(y, psrc, prange)
+    op.combine(y2d, d[1], None, call_reset=True)
+    torch.cuda.synchronize()
+    times = {"dispatch": [], "convert_dispatch_output": [], "convert_combine_input": [],
+             "combine": []}
+    for it in range(W + K):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record(st)
+        d = op.dispatch(x, w, None, idx, ntok)
+        ev[1].record(st)
+        op.convert_dispatch_output(d[0], d[3])
+        ev[2].record(st)
+        op.convert_combine_input(y, psrc, prange, out=y2d)
+        ev[3].record(st)
+        op.combine(y2d, d[1], None, call_reset=True)
+        ev[4].record(st)
+        torch.cuda.synchronize()
+        if it >= W:
+            for j, name in enumerate(times):
+                times[name].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+    peak, _ = hbm_peak()
+    nbytes = {"convert_dispatch_output": C * 2 * H + P * (2 * H + 4),
+              "convert_combine_input": P * 2 * H + C * 2 * H}
+    out = {"workload": wl.name, "copies_C": C, "slots_P": P, "steps": K}
+    for name, ts in times.items():
+        us = statistics.median(ts)
+        rec = {"us_median": round(us, 2)}
+        if name in nbytes:
+            gbs = nbytes[name] / (us * 1e-6) / 1e9
+            rec.update(bytes=nbytes[name], GBps=round(gbs, 1), frac_of_peak=round(gbs / peak, 4))
+        out[name] = rec
+    return out
+
+
 def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -546,6 +608,8 @@ def main():
     ap.add_argument("--workload", default="ds_v3_throughput", choices=sorted(WORKLOADS))
     ap.add_argument("--latency-workload", default="ds_v3_latency")
     ap.add_argument("--combine-impl", default="auto", choices=["auto", "vector", "bulk"])
+    ap.add_argument("--convert", action="store_true",
+                    help="time the 2D path plus the standard-MoE conversions instead")
     ap.add_argument("--launch-mode", default="manual", choices=["manual", "auto"],
                     help="auto: launch parameters from the library's tuning files")
     ap.add_argument("--dispatch-impl", default="auto", choices=["auto", "vector", "bulk"])
@@ -590,6 +654,11 @@ def main():
     if args.sweep:
         if rank == 0:
             print(json.dumps(sweep(wl, dev, args.steps, args.warmup)), flush=True)
+        return
+    if args.convert:
+        if rank == 0:
+            print(json.dumps({"convert_path": convert_leg(wl, dev, args.steps, args.warmup)}),
+                  flush=True)
         return
     barrier = barrier_fn(world)
     step = Step(wl, dev)

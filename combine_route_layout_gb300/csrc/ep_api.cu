@@ -93,6 +93,7 @@ struct Carve {
   uint8_t* packed_x;
   uint8_t* packed_scales;
   uint16_t* conv_local16;
+  int32_t* conv_recv_rows;   // [R][cap][k] packed row of each receive-row slot (conversions)
   int32_t* conv_chunk_cnt;
   int32_t* conv_chunk_off;
   uint8_t* reg_combine_in;   // registered combine input [R][cap][H] (zero-copy mode)
@@ -135,6 +136,7 @@ Carve carve(const Geometry& g, uint8_t* base) {
     take(base, off, c.packed_x, R * g.pcap * g.out_row_bytes);
     take(base, off, c.packed_scales, R * g.pcap * g.scale_row_bytes);
     take(base, off, c.conv_local16, R * g.cap * k * 2);
+    take(base, off, c.conv_recv_rows, R * g.cap * k * 4);
     take(base, off, c.conv_chunk_cnt, (size_t)g.nchunks_recv * g.E_r * 4);
     take(base, off, c.conv_chunk_off, (size_t)g.nchunks_recv * g.E_r * 4);
   }
@@ -704,6 +706,7 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
   p.layout_range = h->w.layout_range;
   p.packed_src_info = h->w.packed_src_info;
   p.row_map = h->w.row_map;
+  p.recv_rows = h->w.conv_recv_rows;
   p.packed_x = h->w.packed_x;
   p.packed_scales = h->w.packed_scales;
   p.ticket = h->w.tickets + 2;
@@ -751,6 +754,7 @@ ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* com
   p.recv_idx = h->w.recv_idx;
   p.src_pos = h->w.src_pos;
   p.row_map = h->w.row_map;
+  p.recv_rows = h->w.conv_recv_rows;
   p.packed_y = static_cast<const uint8_t*>(packed_y);
   p.combine_in = static_cast<uint8_t*>(combine_in);
   cudaError_t e = ep::launch_convert_combine(p, h->cfg.combine_dtype,

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(256) conv_copy_kernel(ConvertParams p) {
         p.packed_src_info[my_row] = pos;
         p.row_map[g * p.k + lane] = (int32_t)my_row;
       }
+      if (lane < p.k) p.recv_rows[rowg * p.k + lane] = (int32_t)my_row;
       if (SCALES) {
         const int nw = p.scale_row_bytes >> 2;
         const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(p.recv_scales + rowg * p.scale_row_bytes);
@@ -207,7 +208,6 @@ template <int DT>
 __global__ void __launch_bounds__(256) conv_combine_kernel(ConvertParams p) {
   const int lane = threadIdx.x & 31;
   constexpr int esz = DT == EP_DTYPE_BF16 ? 2 : 4;
-  const int64_t stride = (int64_t)p.R * p.Tmax;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
        u += nwarps) {
@@ -216,13 +216,9 @@ __global__ void __launch_bounds__(256) conv_combine_kernel(ConvertParams p) {
     const int r = (int)(rowg / p.cap);
     const int64_t i = rowg - (int64_t)r * p.cap;
     if (i >= __ldg(p.recv_num_token + r)) continue;
-    const int pos = __ldg(p.src_pos + rowg);
-    const int64_t g = (pos / stride) * p.Tmax + pos % stride;
-    int prow = -1;
-    if (lane < p.k) {
-      const int e = __ldg(p.recv_idx + rowg * p.k + lane);
-      if (e >= 0 && e / p.E_r == r) prow = __ldg(p.row_map + g * p.k + lane);
-    }
+    // packed rows of this receive row's slots (written by the conversion of
+    // the dispatch output): one load, no token lookup in between
+    const int prow = lane < p.k ? __ldg(p.recv_rows + rowg * p.k + lane) : -1;
     const uint32_t vm = __ballot_sync(kFull, prow >= 0);
     for (int q = 0; q < kCombineUnroll; ++q) {
       const int e0 = (seg * kCombineUnroll + q) * 256 + lane * 8;

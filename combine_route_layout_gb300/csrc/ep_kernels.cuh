@@ -128,6 +128,7 @@ struct ConvertParams {
   int64_t* layout_range;
   int32_t* packed_src_info;
   int32_t* row_map;            // [R*Tmax][k]
+  int32_t* recv_rows;          // [R][cap][k] global packed row of each slot of a receive row, -1
   uint8_t* packed_x;
   uint8_t* packed_scales;
   unsigned int* ticket;
