@@ -544,3 +544,65 @@ def test_fp4_quant_invariants(oracle_lib):
     a = np.abs(x) / np.where(s == 0, 1, s)
     step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
     assert np.all(np.abs(dec - x) <= 0.5 * step * s * (1 + 1e-6) + 1e-30)
+
+
+# ------------------------------------- placement and token-sampled variants
+
+def test_place_rows_against_direct_placement(oracle_lib):
+    """place_rows puts row (s, t) at slot[s, t, r] of every destination r and
+    nothing else (a direct Python placement from the route's slot map);
+    std_place_rows does the same with the packed row map."""
+    wl = WORKLOADS["tiny"].with_(mask_prob=0.2)
+    idx, ntok = make_indices(wl, 3), make_num_tokens(wl, ragged=True, seed=3)
+    R, T, k = idx.shape
+    rows = np.arange(R * T * 3, dtype=np.int32).reshape(R, T, 3) + 1
+    recv, src_pos, slot = oracle_lib.route(idx, ntok, wl.experts_per_rank)
+    got = oracle_lib.place_rows(rows, ntok, slot)
+    want = np.zeros((R, R * T, 3), np.int32)
+    for s in range(R):
+        for t in range(int(ntok[s])):
+            for r in range(R):
+                if slot[s, t, r] >= 0:
+                    want[r, slot[s, t, r]] = rows[s, t]
+    assert np.array_equal(got, want)
+    pcap = R * T * k + 127 * wl.experts_per_rank
+    lay = oracle_lib.std_layout(idx, ntok, wl.experts_per_rank, pcap)
+    got = oracle_lib.std_place_rows(rows, ntok, lay["row_map"], pcap)
+    want = np.zeros((R, pcap, 3), np.int32)
+    for s in range(R):
+        for t in range(int(ntok[s])):
+            for j in range(k):
+                g = lay["row_map"][s, t, j]
+                if g >= 0:
+                    want.reshape(R * pcap, 3)[g] = rows[s, t]
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("weighted,od", [(False, "bf16"), (True, "fp32")])
+def test_combine_tokens_equals_combine_rows(oracle_lib, weighted, od):
+    """The token-sampled combines give exactly the rows of the full ones (which
+    the identity invariants and exact sums above pin), in the order asked."""
+    wl = WORKLOADS["tiny"].with_(mask_prob=0.1)
+    idx, ntok = make_indices(wl, 4), make_num_tokens(wl, ragged=True, seed=4)
+    R, T, k = idx.shape
+    w = make_weights(wl, 4)
+    rng = np.random.default_rng(4)
+    recv, src_pos, slot = oracle_lib.route(idx, ntok, wl.experts_per_rank)
+    y = rng.standard_normal((R, R * T, wl.hidden)).astype(np.float32)
+    w_recv = oracle_lib.place_rows(w, ntok, slot)
+    full, full_w = oracle_lib.combine(y, idx, ntok, slot, wl.experts_per_rank, w_recv=w_recv,
+                                      weighted=weighted, out_dtype=od)
+    toks = np.array([s * T + t for s in range(R) for t in range(int(ntok[s]))], np.int64)
+    toks = toks[rng.permutation(len(toks))]
+    part, part_w = oracle_lib.combine_tokens(toks, y, idx, slot, wl.experts_per_rank,
+                                             w_recv=w_recv, weighted=weighted, out_dtype=od)
+    assert np.array_equal(part, full[toks // T, toks % T])
+    assert np.array_equal(part_w, full_w[toks // T, toks % T])
+    pcap = R * T * k + 127 * wl.experts_per_rank
+    lay = oracle_lib.std_layout(idx, ntok, wl.experts_per_rank, pcap)
+    Y = rng.standard_normal((R, pcap, wl.hidden)).astype(np.float32)
+    sfull = oracle_lib.std_combine(Y, idx, ntok, lay["row_map"], wl.experts_per_rank, w=w,
+                                   weighted=weighted, out_dtype=od)
+    spart = oracle_lib.std_combine_tokens(toks, Y, idx, lay["row_map"], wl.experts_per_rank,
+                                          w=w, weighted=weighted, out_dtype=od)
+    assert np.array_equal(spart, sfull[toks // T, toks % T])
