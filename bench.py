@@ -76,13 +76,16 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel_key: str):
+def profiled_traffic(kernel_key: str, workload: str | None = None):
     """Per-launch DRAM bytes from a committed ncu summary, if the kernel
-    source has not changed since it was captured."""
+    source has not changed since it was captured (and, when given, the
+    summary is of this workload)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)[kernel_key]
+        if workload is not None and rec["workload"].split()[0] != workload:
+            return None
         src = os.path.join(ROOT, rec["source"])
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if h != rec["source_sha256_16"]:
@@ -682,7 +685,7 @@ def main():
                "dispatch": "dispatch_2d" if not wl.standard_moe else "dispatch_std"}[dom]
     dom_kernel = chosen_kernels(step)[dom]
     ach = c_gbs if dom == "combine" else d_gbs
-    tr = profiled_traffic(dom_key)
+    tr = profiled_traffic(dom_key, wl.name)
     if tr and not tr["kernel"].startswith(dom_kernel.replace("_kernel", "")):
         tr = None
     line = {
