@@ -249,8 +249,20 @@ int ep::ctas_per_sm(const void* kernel, int block, size_t smem) {
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  if (smem > 48 * 1024)
-    (void)cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem > 48 * 1024) {
+    // the limit is a property of the kernel, not of one launch: raise it to the
+    // device maximum (less the kernel's static shared memory) so launches of
+    // other sizes keep working
+    int optin = 0;
+    cudaFuncAttributes fa{};
+    if (dev < 0 ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
+      optin = 0;
+    const int most = optin - (int)fa.sharedSizeBytes;
+    (void)cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               most > (int)smem ? most : (int)smem);
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess ||
       n < 1)

@@ -3,8 +3,12 @@
 //
 // MORI-EP User Guide, section 3, combine() and section 4,
 // combine_standard_moe(); "Choosing an EP API and backend": gather combine in
-// BF16/FP32. A unit is (source token, 1024-column chunk); each CTA takes
-// whole tokens, all chunks in a row. One producer warp per CTA reads the
+// BF16/FP32. A unit is (source token, 1024-column chunk). A CTA takes
+// whole tokens c, c + G, c + 2G, ... (G CTAs), all chunks of each; or, for
+// small batches, a contiguous balanced range of units over the present
+// tokens (at most one unit more than any other CTA, so a batch of a few
+// thousand units has no tail of CTAs with a whole extra token). One
+// producer warp per CTA reads the
 // token's slot row once (the next token's is prefetched meanwhile), orders
 // the token's rows (ascending destination rank; or owner rank then slot for
 // the packed layout) and, per chunk, has each lane with a row issue one
@@ -29,6 +33,7 @@ constexpr int kStages = 4;       // units in flight per CTA
 constexpr int kRows = 8;         // at most 8 rows per unit
 constexpr int kConsumers = 4;    // 128 consumer threads x 8 columns = kCols
 constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int64_t kBalancedMaxUnits = 64;  // units per CTA up to which ranges are balanced
 
 constexpr int esize(int dt) { return dt == EP_DTYPE_BF16 ? 2 : 4; }
 
@@ -80,7 +85,7 @@ __device__ __forceinline__ void unpack_smem8(const uint8_t* src, float f[8]) {
 }
 
 template <bool STD, int IN, int OUT>
-__global__ void __launch_bounds__(kThreads) combine_bulk_kernel(CombineParams p) {
+__global__ void __launch_bounds__(kThreads, 3) combine_bulk_kernel(CombineParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Ring<IN>& ring = *reinterpret_cast<Ring<IN>*>(smem_raw);
   constexpr int esz = esize(IN);
@@ -94,36 +99,48 @@ __global__ void __launch_bounds__(kThreads) combine_bulk_kernel(CombineParams p)
   }
   __syncthreads();
   const int segs = p.segs_per_token;
-
-  const int64_t ntokens = (int64_t)p.R * p.Tmax;
-  auto present = [&](int64_t g) {
-    const int s = (int)(g / p.Tmax);
-    return (int)(g - (int64_t)s * p.Tmax) < p.ntok[s];
+  const int64_t T = p.tok_prefix[p.R];   // present tokens
+  // This CTA's units in (token, chunk) order. Balanced: units [u0, u1) over
+  // the present tokens. Token-stride: every chunk of tokens c, c + G, ...
+  const int64_t U = p.total_units;
+  const int64_t u0 = p.balanced ? (int64_t)blockIdx.x * U / gridDim.x : (int64_t)blockIdx.x * segs;
+  const int64_t u1 = p.balanced ? (int64_t)(blockIdx.x + 1) * U / gridDim.x : U;
+  const int64_t vstep = p.balanced ? 1 : gridDim.x;
+  const int64_t nunits =
+      p.balanced ? u1 - u0 : (blockIdx.x < T ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0) * segs;
+  // global token index of the v-th present token
+  auto token_of = [&](int64_t v) -> int64_t {
+    int s = 0;
+    while (s + 1 < p.R && v >= p.tok_prefix[s + 1]) ++s;
+    return (int64_t)s * p.Tmax + (v - p.tok_prefix[s]);
   };
 
   if (warp == kConsumers) {  // ------------------------------------- producer
-    // Slot entry of `lane` for token g: receive slot on rank `lane` (2D) or
-    // packed row of slot `lane` (standard MoE); -1 when absent.
-    auto slot_of = [&](int64_t g) -> int {
-      if (g >= ntokens || !present(g)) return -1;
+    // Slot entry of `lane` for present token v: receive slot on rank `lane`
+    // (2D) or packed row of slot `lane` (standard MoE); -1 when absent or
+    // past this CTA's units.
+    auto mine = [&](int64_t v) { return v < T && v * segs < u1; };
+    auto slot_of = [&](int64_t v) -> int {
+      if (!mine(v)) return -1;
+      const int64_t g = token_of(v);
       if (!STD) return lane < p.R ? __ldg(p.slot_map + g * p.R + lane) : -1;
       return lane < p.k ? __ldg(p.row_map + g * p.k + lane) : -1;
     };
-    auto weight_of = [&](int64_t g) -> float {  // standard MoE: router weight of slot `lane`
-      if (!STD || !p.weighted || g >= ntokens || lane >= p.k || !present(g)) return 0.0f;
-      return __ldg(p.w + g * p.k + lane);
+    auto weight_of = [&](int64_t v) -> float {  // standard MoE: router weight of slot `lane`
+      if (!STD || !p.weighted || !mine(v) || lane >= p.k) return 0.0f;
+      return __ldg(p.w + token_of(v) * p.k + lane);
     };
     int i = 0;
     bool failed = false;
-    int64_t g = blockIdx.x;
-    int sl_next = slot_of(g);
-    float w_next = weight_of(g);
-    for (; g < ntokens && !failed; g += gridDim.x) {
+    int64_t v = u0 / segs;
+    int sl_next = slot_of(v);
+    float w_next = weight_of(v);
+    for (; i < nunits && !failed; v += vstep) {
+      const int64_t g = token_of(v);
       const int sl = sl_next;
       const float wslot = w_next;
-      sl_next = slot_of(g + gridDim.x);       // prefetch the next token's slot row
-      w_next = weight_of(g + gridDim.x);
-      if (!present(g)) continue;
+      sl_next = slot_of(v + vstep);   // prefetch the next token's slot row
+      w_next = weight_of(v + vstep);
       // rows of this token, their order d and (weighted) their weights
       int d = -1;
       int64_t row = -1;
@@ -153,7 +170,9 @@ __global__ void __launch_bounds__(kThreads) combine_bulk_kernel(CombineParams p)
         }
       }
       const int D = __popc(m);
-      for (int seg = 0; seg < segs; ++seg, ++i) {
+      const int seg0 = (int)(max(u0, v * segs) - v * segs);
+      const int seg1 = (int)(min(u1, (v + 1) * segs) - v * segs);
+      for (int seg = seg0; seg < seg1; ++seg, ++i) {
         const int st = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
         if (i >= kStages && !mbar_wait(&ring.empty[st], ph ^ 1u)) {
@@ -164,6 +183,8 @@ __global__ void __launch_bounds__(kThreads) combine_bulk_kernel(CombineParams p)
         const uint32_t bytes = (uint32_t)(min(kCols, p.H - seg * kCols) * esz);
         StageHdr& h = ring.hdr[st];
         if (lane == 0) {
+          h.g = g;
+          h.seg = seg;
           h.D = D;
           h.rmin = rmin;
           h.slmin = slmin;
@@ -192,42 +213,39 @@ __global__ void __launch_bounds__(kThreads) combine_bulk_kernel(CombineParams p)
 
   // ----------------------------------------------------------------- consumers
   const int tid = threadIdx.x;  // 0 .. 127
-  int i = 0;
-  for (int64_t g = blockIdx.x; g < ntokens; g += gridDim.x) {
-    if (!present(g)) continue;
-    for (int seg = 0; seg < segs; ++seg, ++i) {
-      const int st = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-      if (!mbar_wait(&ring.full[st], ph)) {
-        if (lane == 0) atomicOr(p.err, kErrTimeout);
-        return;
-      }
-      const StageHdr& h = ring.hdr[st];
-      const int D = h.D;
-      const int col = seg * kCols + tid * 8;
-      if (col < p.H) {
-        float acc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-#pragma unroll
-        for (int d = 0; d < kRows; ++d) {
-          if (d < D) {
-            float f[8];
-            unpack_smem8<IN>(ring.data[st][d] + tid * 8 * esz, f);
-            const float wd = h.w[d];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              acc[q] = p.weighted ? __fmaf_rn(wd, f[q], acc[q]) : __fadd_rn(acc[q], f[q]);
-          }
-        }
-        store8<OUT>(p.out + g * p.H * esize(OUT), col, acc);
-      }
-      if (!STD && seg == 0 && p.out_w && warp == 0 && lane < p.k)
-        p.out_w[g * p.k + lane] =
-            D > 0 ? __ldg(p.w + ((int64_t)h.rmin * p.cap + h.slmin) * p.k + lane) : 0.0f;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[st]);
+  for (int i = 0; i < nunits; ++i) {
+    const int st = i % kStages;
+    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    if (!mbar_wait(&ring.full[st], ph)) {
+      if (lane == 0) atomicOr(p.err, kErrTimeout);
+      return;
     }
+    const StageHdr& h = ring.hdr[st];
+    const int D = h.D, seg = h.seg;
+    const int64_t g = h.g;
+    const int col = seg * kCols + tid * 8;
+    if (col < p.H) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+      for (int d = 0; d < kRows; ++d) {
+        if (d < D) {
+          float f[8];
+          unpack_smem8<IN>(ring.data[st][d] + tid * 8 * esz, f);
+          const float wd = h.w[d];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            acc[q] = p.weighted ? __fmaf_rn(wd, f[q], acc[q]) : __fadd_rn(acc[q], f[q]);
+        }
+      }
+      store8<OUT>(p.out + g * p.H * esize(OUT), col, acc);
+    }
+    if (!STD && seg == 0 && p.out_w && warp == 0 && lane < p.k)
+      p.out_w[g * p.k + lane] =
+          D > 0 ? __ldg(p.w + ((int64_t)h.rmin * p.cap + h.slmin) * p.k + lane) : 0.0f;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[st]);
   }
 }
 
@@ -236,7 +254,9 @@ cudaError_t launch_bulk(const CombineParams& p0, int in_dtype, int out_dtype, co
                         cudaStream_t st) {
   CombineParams p = p0;
   p.segs_per_token = (p.H + kCols - 1) / kCols;
-  p.total_units = (int64_t)p.R * p.Tmax * p.segs_per_token;
+  p.tok_prefix[0] = 0;
+  for (int s = 0; s < p.R; ++s) p.tok_prefix[s + 1] = p.tok_prefix[s] + p.ntok[s];
+  p.total_units = (int64_t)p.tok_prefix[p.R] * p.segs_per_token;
   if (p.total_units == 0) return cudaSuccess;
   const bool ib = in_dtype == EP_DTYPE_BF16, ob = out_dtype == EP_DTYPE_BF16;
   void (*k)(CombineParams) =
@@ -247,8 +267,10 @@ cudaError_t launch_bulk(const CombineParams& p0, int in_dtype, int out_dtype, co
   const size_t smem = ib ? sizeof(Ring<EP_DTYPE_BF16>) : sizeof(Ring<EP_DTYPE_FP32>);
   const int per_sm = ctas_per_sm(k, kThreads, smem);  // also raises the smem limit
   int64_t grid = lc.grid_hint > 0 ? lc.grid_hint : (int64_t)lc.sm_count * per_sm;
-  const int64_t ntokens = (int64_t)p.R * p.Tmax;
-  if (grid > ntokens) grid = ntokens;
+  // balanced ranges while a CTA has few units (a token more or less is a
+  // large share of its work); whole tokens per CTA otherwise
+  p.balanced = p.total_units <= grid * kBalancedMaxUnits;
+  if (grid > (p.balanced ? p.total_units : p.tok_prefix[p.R])) grid = p.balanced ? p.total_units : p.tok_prefix[p.R];
   k<<<(unsigned)grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }

@@ -102,6 +102,10 @@ struct CombineParams {
   uint8_t* out;
   float* out_w;
   int32_t* err;
+  // bulk kernel: exclusive prefix of ntok (present tokens before rank s), and
+  // the work order (1: balanced unit ranges per CTA; 0: whole tokens, strided)
+  int tok_prefix[EP_MAX_WORLD_SIZE + 1] = {};
+  int balanced = 0;
 };
 
 struct ConvertParams {

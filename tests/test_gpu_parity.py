@@ -121,8 +121,11 @@ def test_tiny_identity(seed, ragged):
     run_2d(WORKLOADS["tiny"], seed=seed, ragged=ragged)
 
 
-def test_ds_v3_latency_full():
-    run_2d(WORKLOADS["ds_v3_latency"])
+@pytest.mark.parametrize("impl", ["auto", "vector"])
+def test_ds_v3_latency_full(impl):
+    """The decode shape whole, with the automatic and the forced-vector
+    dispatch choice."""
+    run_2d(WORKLOADS["ds_v3_latency"], cfg_over=dict(dispatch_impl=impl))
 
 
 @pytest.mark.parametrize("seed", [1, 2])
@@ -583,7 +586,8 @@ def test_bulk_combine_full_size():
 
 # ------------------------------------------------------------- codec sweeps
 
-def test_gpu_e4m3_codes_for_every_bf16_value():
+@pytest.mark.parametrize("impl", ["auto", "vector"])
+def test_gpu_e4m3_codes_for_every_bf16_value(impl):
     """Every finite bf16 value with |x| <= 448 passes through the FP8 dispatch
     with a block scale of exactly 1 (each block holds 448), so the codes are
     E4M3(x) and must equal the oracle's encoder."""
@@ -606,7 +610,7 @@ def test_gpu_e4m3_codes_for_every_bf16_value():
                                  hidden=H, dispatch_dtype="fp8", expert_output="random")
     idx = np.zeros((R, T, 1), np.int32)
     w = np.ones((R, T, 1), np.float32)
-    op = EpDispatchCombineOp(make_config(wl))
+    op = EpDispatchCombineOp(make_config(wl, dispatch_impl=impl))
     xd = torch.from_numpy(x.view(np.int16)).to(DEV).view(torch.bfloat16)
     d_x, _, d_sc, _, recv = op.dispatch(xd, torch.from_numpy(w).to(DEV), None,
                                          torch.from_numpy(idx).to(DEV), [T])
@@ -723,13 +727,15 @@ def test_bulk_dispatch_full_size():
 
 # --------------------------------------------------------------- FP4 dispatch
 
+@pytest.mark.parametrize("impl", ["auto", "vector"])
 @pytest.mark.parametrize("over,seed", [(dict(), 0), (dict(tokens_per_rank=300, hidden=1056), 1),
                                        (dict(tokens_per_rank=70, hidden=224), 2)])
-def test_fp4_dispatch(over, seed):
+def test_fp4_dispatch(over, seed, impl):
     """FP4 E2M1 block-32 quantisation in dispatch: codes, nibble order and
-    scales bit-exact against the oracle (2D layout)."""
+    scales bit-exact against the oracle (2D layout), automatic and forced-vector
+    dispatch choice."""
     wl = WORKLOADS["ds_v3_latency"].with_(dispatch_dtype="fp4").with_(**over)
-    run_2d(wl, seed=seed, ragged=bool(seed))
+    run_2d(wl, seed=seed, ragged=bool(seed), cfg_over=dict(dispatch_impl=impl))
 
 
 def test_fp4_dispatch_standard_moe():
@@ -927,7 +933,7 @@ def test_small_batch_chunk_offsets(name, over, seed):
 
 # ------------------------------- quantisation with arbitrary (inexact) scales
 
-def _quant_sweep(fmt, amax_bits):
+def _quant_sweep(fmt, amax_bits, impl="auto"):
     """Every finite bf16 value with |x| <= amax in blocks whose amax is fixed,
     for each amax in amax_bits: codes and scales from dispatch against the
     oracle's encoder, bit for bit."""
@@ -955,7 +961,7 @@ def _quant_sweep(fmt, amax_bits):
     x = xx.reshape(1, T, H)
     wl = WORKLOADS["tiny"].with_(world_size=1, experts_per_rank=1, topk=1, tokens_per_rank=T,
                                  hidden=H, dispatch_dtype=fmt, expert_output="random")
-    op = EpDispatchCombineOp(make_config(wl))
+    op = EpDispatchCombineOp(make_config(wl, dispatch_impl=impl))
     xd = torch.from_numpy(x.view(np.int16)).to(DEV).view(torch.bfloat16)
     w = torch.ones((1, T, 1), dtype=torch.float32, device=DEV)
     idx = torch.zeros((1, T, 1), dtype=torch.int32, device=DEV)
@@ -971,8 +977,9 @@ def _bf16_bits(v):
     return int((np.array([v], np.float32).view(np.uint32)[0] + 0x8000) >> 16)
 
 
+@pytest.mark.parametrize("impl", ["auto", "vector"])
 @pytest.mark.parametrize("fmt", ["fp8", "fp4"])
-def test_quant_codes_every_bf16_value_inexact_scales(fmt):
+def test_quant_codes_every_bf16_value_inexact_scales(fmt, impl):
     """Codes of the correctly rounded quotient for every input: all finite
     bf16 values under amax values whose scale amax/448 (or amax/6) is inexact,
     exact, a power of two, below 2^-90 or above 2^125, or subnormal."""
@@ -981,7 +988,75 @@ def test_quant_codes_every_bf16_value_inexact_scales(fmt):
     amax += [_bf16_bits(v) for v in (448.0, 6.0, 448.0 * 2.0 ** -40, 6.0 * 2.0 ** 20, 1e-25)]
     amax += [int(b) for b in (rng.integers(0x0080, 0x7F7F, size=6))]     # random finite positives
     amax += [0x0001, 0x0050, 0x0100, 0x7F7F, 0x7F00]                      # tiny scales, huge amax
-    _quant_sweep(fmt, amax)
+    _quant_sweep(fmt, amax, impl)
+
+
+def _blocks_every_amax(a_lo: int, a_hi: int, blk: int, binades: int = 24) -> np.ndarray:
+    """bf16 bits of blocks of `blk` elements: for every positive finite bf16
+    block maximum a in [a_lo, a_hi) (bit patterns), every bf16 x of either sign
+    with |x| <= a and |x| in the `binades` binades below a, plus zeros; the
+    last element of each block is a itself. Values per maximum are padded
+    with +0 to whole blocks."""
+    per = blk - 1
+    a = np.arange(a_lo, a_hi, dtype=np.int64)
+    lo = np.maximum(1, a - 128 * binades)
+    n = 2 * (a - lo + 1) + 2                     # +/- each magnitude, and +/-0
+    nblk = -(-n // per)
+    out = np.zeros((int(nblk.sum()), blk), np.uint16)
+    out[:, per] = np.repeat(a, nblk).astype(np.uint16)
+    vals = np.zeros(int((nblk * per).sum()), np.uint16)
+    start = np.concatenate([[0], np.cumsum(nblk * per)[:-1]])
+    for j in range(len(a)):                       # (a_hi - a_lo) is small per chunk
+        mags = np.arange(lo[j], a[j] + 1, dtype=np.uint16)
+        v = np.concatenate([mags, mags | np.uint16(0x8000), np.array([0, 0x8000], np.uint16)])
+        vals[start[j]:start[j] + len(v)] = v
+    out[:, :per] = vals.reshape(-1, per)
+    return out.reshape(-1)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+def test_quant_codes_every_block_maximum(fmt):
+    """A code depends only on the element and its block's maximum (the scale
+    is amax / 448 or amax / 6). For every positive finite bf16 block maximum
+    and every bf16 element of either sign in the 24 binades below it (smaller
+    elements quote far below half the smallest nonzero code), dispatch's
+    codes and scales equal the oracle's, which divides with IEEE rounding:
+    the kernel's reciprocal-and-residual quotient (taken below 8192 source
+    tokens for FP8, always for FP4) is checked on every input pair whose code
+    it can decide."""
+    blk = 128 if fmt == "fp8" else 32
+    H = 1024
+    T = 4096   # below 8192 tokens FP8 dispatch takes the reciprocal-and-residual quotients
+    wl = WORKLOADS["tiny"].with_(world_size=1, experts_per_rank=1, topk=1, tokens_per_rank=T,
+                                 hidden=H, dispatch_dtype=fmt, expert_output="random")
+    op = EpDispatchCombineOp(make_config(wl))
+    w = torch.ones((1, T, 1), dtype=torch.float32, device=DEV)
+    idx = torch.zeros((1, T, 1), dtype=torch.int32, device=DEV)
+    quant = oracle.quant_tokens if fmt == "fp8" else oracle.quant_tokens_fp4
+    pending = np.zeros(0, np.uint16)
+    a_next, a_end = 1, 0x7F80                     # every positive finite bf16
+    checked = 0
+    while a_next < a_end or pending.size:
+        while pending.size < T * H and a_next < a_end:
+            hi = min(a_end, a_next + 256)
+            pending = np.concatenate([pending, _blocks_every_amax(a_next, hi, blk)])
+            a_next = hi
+        x = np.zeros(T * H, np.uint16)
+        m = min(pending.size, T * H)
+        x[:m] = pending[:m]
+        pending = pending[m:]
+        ntok = -(-m // H)
+        xd = torch.from_numpy(x.view(np.int16)).to(DEV).view(torch.bfloat16).view(1, T, H)
+        d_x, _, d_sc, _, _ = op.dispatch(xd, w, None, idx, [ntok])
+        op.sync()
+        xs = x.reshape(1, T, H)[:, :ntok]
+        q_ref, sc_ref = quant(np.ascontiguousarray(xs))
+        assert np.array_equal(host(d_sc)[0, :ntok].view(np.uint32), sc_ref[0].view(np.uint32))
+        assert np.array_equal(host(d_x)[0, :ntok], q_ref[0]), "codes"
+        op.reset()
+        checked += m
+    assert checked > 150_000_000
 
 
 # ---------------------------------------- launch configuration and tuning files
