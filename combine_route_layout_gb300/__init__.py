@@ -7,11 +7,15 @@ library exists; any other use fails loudly if the library is missing.
 """
 
 _EXPORTS = ("EpDispatchCombineConfig", "EpDispatchCombineOp", "EpError")
+_RANK_EXPORTS = ("EpRankOp", "exchange_workspaces", "phase_barrier")
 
 
 def __getattr__(name):
+    import importlib
     if name == "ep" or name in _EXPORTS:
-        import importlib
         ep = importlib.import_module(".ep", __name__)
         return ep if name == "ep" else getattr(ep, name)
+    if name == "ranks" or name in _RANK_EXPORTS:
+        ranks = importlib.import_module(".ranks", __name__)
+        return ranks if name == "ranks" else getattr(ranks, name)
     raise AttributeError(name)

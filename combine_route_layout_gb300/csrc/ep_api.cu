@@ -841,3 +841,402 @@ ep_status ep_sync(ep_handle* h, void* stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// One EP rank per workspace, split send / receive phases (MORI-EP User
+// Guide, section 3, "Split dispatch/combine (send + recv)"). The kernels are
+// in ep_split.cu; this is the workspace layout, the peer table and the
+// per-rank state machine.
+
+namespace {
+
+enum RankState { kRReady = 0, kRSent = 1, kRDispatched = 2, kRCombineSent = 3, kRCombined = 4 };
+
+struct RankCarve {
+  int32_t* err;
+  unsigned int* tickets;
+  uint32_t* mask;            // [Tmax]
+  uint8_t* local8;           // [Tmax][R]
+  int32_t* chunk_cnt;        // [cpr][R]
+  int32_t* chunk_off;        // [cpr][R]
+  int32_t* send_cnt;         // [R] own tokens sent to each rank
+  int32_t* slot_own;         // [Tmax][R]
+  int32_t* send_list;        // [R][Tmax]
+  uint8_t* send_x;           // [Tmax][out_row_bytes]
+  uint8_t* send_scales;      // [Tmax][scale_row_bytes]
+  float* send_w;             // [Tmax][k]
+  int32_t* send_idx;         // [Tmax][k]
+  int32_t* recv_off;         // [R]
+  int32_t* recv_num_token;   // [1]
+  int32_t* src_pos;          // [cap]
+  uint8_t* recv_x;           // [cap][out_row_bytes]
+  uint8_t* recv_scales;      // [cap][scale_row_bytes]
+  float* recv_w;             // [cap][k]
+  int32_t* recv_idx;         // [cap][k]
+  uint8_t* reg_combine_in;   // [cap][H] combine_dtype
+  float* comb_w;             // [cap][k] weights given to combine_send
+  size_t total;
+};
+
+RankCarve carve_rank(const Geometry& g, uint8_t* base) {
+  RankCarve c{};
+  size_t off = 0;
+  const int64_t R = g.R, T = g.Tmax, k = g.k;
+  take(base, off, c.err, 4 * sizeof(int32_t));
+  take(base, off, c.tickets, 4 * sizeof(unsigned int));
+  take(base, off, c.mask, T * 4);
+  take(base, off, c.local8, T * R);
+  take(base, off, c.chunk_cnt, (size_t)g.cpr * R * 4);
+  take(base, off, c.chunk_off, (size_t)g.cpr * R * 4);
+  take(base, off, c.send_cnt, R * 4);
+  take(base, off, c.slot_own, T * R * 4);
+  take(base, off, c.send_list, R * T * 4);
+  take(base, off, c.send_x, T * g.out_row_bytes);
+  take(base, off, c.send_scales, T * g.scale_row_bytes);
+  take(base, off, c.send_w, T * k * 4);
+  take(base, off, c.send_idx, T * k * 4);
+  take(base, off, c.recv_off, R * 4);
+  take(base, off, c.recv_num_token, 4);
+  take(base, off, c.src_pos, g.cap * 4);
+  take(base, off, c.recv_x, g.cap * g.out_row_bytes);
+  take(base, off, c.recv_scales, g.cap * g.scale_row_bytes);
+  take(base, off, c.recv_w, g.cap * k * 4);
+  take(base, off, c.recv_idx, g.cap * k * 4);
+  take(base, off, c.reg_combine_in, g.cap * g.combine_in_row_bytes);
+  take(base, off, c.comb_w, g.cap * k * 4);
+  c.total = off;
+  return c;
+}
+
+ep_status make_rank_geometry(const ep_config* cfg, Geometry* g) {
+  ep_status s = make_geometry(cfg, g);
+  if (s != EP_OK) return s;
+  if (g->std_moe)
+    return fail(EP_ERR_UNSUPPORTED, "the split send/receive phases use the 2D layout (standard_moe = 0)");
+  if (g->scale_row_bytes % 4 != 0)
+    return fail(EP_ERR_UNSUPPORTED, "the split phases need scale rows that are a multiple of 4 bytes");
+  return EP_OK;
+}
+
+}  // namespace
+
+struct ep_rank_handle {
+  ep_config cfg;
+  Geometry g;
+  RankCarve w;
+  int rank;
+  uint8_t* ws;
+  const uint8_t* peers[EP_MAX_WORLD_SIZE];
+  bool has_peers;
+  int state;
+  bool needs_init;
+  int ntok;
+  int sm_count;
+  uint8_t* out;              // combine_send's output buffers, written by combine_recv
+  float* out_w;
+  bool weighted_w;           // combine_send was given weights
+};
+
+namespace {
+
+ep_status rank_ready_device(ep_rank_handle* h, cudaStream_t st) {
+  if (h->sm_count == 0) {
+    ep_status s = device_sm_count(&h->sm_count);
+    if (s != EP_OK) return s;
+  }
+  if (h->needs_init) {
+    cudaError_t e = cudaMemsetAsync(h->w.err, 0, 4 * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->w.tickets, 0, 4 * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    h->needs_init = false;
+  }
+  return EP_OK;
+}
+
+ep::LaunchCfg rank_launch_cfg(const ep_rank_handle* h) {
+  ep::LaunchCfg lc;
+  lc.grid_hint = h->cfg.block_num;
+  lc.block = (h->cfg.warp_num_per_block > 0 ? h->cfg.warp_num_per_block : 8) * 32;
+  lc.sm_count = h->sm_count;
+  return lc;
+}
+
+ep::SplitPeers rank_peers(const ep_rank_handle* h) {
+  ep::SplitPeers pe{};
+  for (int r = 0; r < h->g.R; ++r) pe.base[r] = h->peers[r];
+  pe.rank = h->rank;
+  const uint8_t* b = h->ws;
+  auto off = [b](const void* p) { return (int64_t)(static_cast<const uint8_t*>(p) - b); };
+  pe.off_send_cnt = off(h->w.send_cnt);
+  pe.off_send_list = off(h->w.send_list);
+  pe.off_send_x = off(h->w.send_x);
+  pe.off_send_scales = off(h->w.send_scales);
+  pe.off_send_w = off(h->w.send_w);
+  pe.off_send_idx = off(h->w.send_idx);
+  pe.off_recv_off = off(h->w.recv_off);
+  pe.off_y = off(h->w.reg_combine_in);
+  pe.off_w = off(h->w.comb_w);
+  return pe;
+}
+
+void rank_split_params(const ep_rank_handle* h, ep::SplitParams* p) {
+  const Geometry& g = h->g;
+  memset(p, 0, sizeof(*p));
+  p->R = g.R; p->Tmax = g.Tmax; p->k = g.k; p->E_r = g.E_r; p->E = g.E; p->H = g.H;
+  p->ntok = h->ntok;
+  p->cap = g.cap;
+  p->in_row_bytes = g.in_row_bytes;
+  p->out_row_bytes = g.out_row_bytes;
+  p->scale_row_bytes = g.scale_row_bytes;
+  p->in_scale_row_bytes = g.quant ? 0 : g.in_scale_row_bytes;
+  const int64_t step = g.quant ? (int64_t)ep::kQuantUnroll * 512 * 2 : (int64_t)ep::kCopyUnroll * 512;
+  p->segs_per_token = (int)((g.in_row_bytes + step - 1) / step);
+  p->segs_per_row = (int)((g.out_row_bytes + ep::kCopyUnroll * 512 - 1) / (ep::kCopyUnroll * 512));
+  p->total_units = (int64_t)h->ntok * p->segs_per_token;
+  p->mask = h->w.mask;
+  p->local8 = h->w.local8;
+  p->chunk_off = h->w.chunk_off;
+  p->slot_own = h->w.slot_own;
+  p->send_list = h->w.send_list;
+  p->send_x = h->w.send_x;
+  p->send_scales = h->w.send_scales;
+  p->send_w = h->w.send_w;
+  p->send_idx = h->w.send_idx;
+  p->recv_x = h->w.recv_x;
+  p->recv_scales = h->w.recv_scales;
+  p->recv_w = h->w.recv_w;
+  p->recv_idx = h->w.recv_idx;
+  p->src_pos = h->w.src_pos;
+  p->recv_off = h->w.recv_off;
+  p->recv_num_token = h->w.recv_num_token;
+  p->err = h->w.err;
+}
+
+void fill_rank_dispatch_out(const ep_rank_handle* h, ep_dispatch_out* out) {
+  if (!out) return;
+  out->x = h->w.recv_x;
+  out->scales = h->g.scale_row_bytes > 0 ? h->w.recv_scales : nullptr;
+  out->weights = h->w.recv_w;
+  out->indices = h->w.recv_idx;
+  out->recv_num_token = h->w.recv_num_token;
+  out->src_token_pos = h->w.src_pos;
+  out->cap = h->g.cap;
+  out->x_row_bytes = h->g.out_row_bytes;
+  out->scale_row_bytes = h->g.scale_row_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ep_rank_workspace_size(const ep_config* cfg) {
+  Geometry g;
+  if (make_rank_geometry(cfg, &g) != EP_OK) return 0;
+  return carve_rank(g, nullptr).total;
+}
+
+ep_status ep_rank_create(const ep_config* cfg, int32_t rank, void* d_workspace,
+                         size_t workspace_bytes, ep_rank_handle** out_handle) {
+  if (!out_handle) return fail(EP_ERR_INVALID_ARG, "out_handle is NULL");
+  *out_handle = nullptr;
+  Geometry g;
+  ep_status s = make_rank_geometry(cfg, &g);
+  if (s != EP_OK) return s;
+  if (rank < 0 || rank >= g.R)
+    return fail(EP_ERR_INVALID_ARG, "rank %d outside [0, %d)", rank, g.R);
+  const size_t need = carve_rank(g, nullptr).total;
+  if (!d_workspace) return fail(EP_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(d_workspace, kAlign)) return fail(EP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (workspace_bytes < need)
+    return fail(EP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  ep_rank_handle* h = new ep_rank_handle();
+  h->cfg = *cfg;
+  h->g = g;
+  h->rank = rank;
+  h->ws = static_cast<uint8_t*>(d_workspace);
+  h->w = carve_rank(g, h->ws);
+  for (int r = 0; r < EP_MAX_WORLD_SIZE; ++r) h->peers[r] = nullptr;
+  h->peers[rank] = h->ws;
+  h->has_peers = g.R == 1;
+  h->state = kRReady;
+  h->needs_init = true;
+  h->sm_count = 0;
+  *out_handle = h;
+  return EP_OK;
+}
+
+void ep_rank_destroy(ep_rank_handle* h) { delete h; }
+
+ep_status ep_rank_set_peers(ep_rank_handle* h, void* const* peer_workspaces) {
+  if (!h || !peer_workspaces) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+  if (h->state != kRReady) return fail(EP_ERR_STATE, "peers can change only between iterations");
+  for (int r = 0; r < h->g.R; ++r) {
+    if (!peer_workspaces[r]) return fail(EP_ERR_INVALID_ARG, "peer workspace %d is NULL", r);
+    if (!aligned(peer_workspaces[r], kAlign))
+      return fail(EP_ERR_INVALID_ARG, "peer workspace %d is not 256-byte aligned", r);
+  }
+  if (peer_workspaces[h->rank] != h->ws)
+    return fail(EP_ERR_INVALID_ARG, "entry %d must be this rank's own workspace", h->rank);
+  for (int r = 0; r < h->g.R; ++r) h->peers[r] = static_cast<const uint8_t*>(peer_workspaces[r]);
+  h->has_peers = true;
+  return EP_OK;
+}
+
+ep_status ep_dispatch_send(ep_rank_handle* h, const void* x, const float* weights,
+                           const void* scales, const int32_t* indices, int32_t num_tokens,
+                           void* stream, ep_dispatch_out* out) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (h->state != kRReady) return fail(EP_ERR_STATE, "dispatch_send needs reset() after the previous iteration");
+  const Geometry& g = h->g;
+  if (num_tokens < 0 || num_tokens > g.Tmax)
+    return fail(EP_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, g.Tmax);
+  if (!x || !weights || !indices) return fail(EP_ERR_INVALID_ARG, "x, weights and indices must be non-NULL");
+  if (!aligned(x, 16)) return fail(EP_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  if (!aligned(weights, 4) || !aligned(indices, 4))
+    return fail(EP_ERR_INVALID_ARG, "weights and indices must be 4-byte aligned");
+  if (g.quant && scales) return fail(EP_ERR_INVALID_ARG, "scales must be NULL with block quantisation (computed)");
+  if (!g.quant && g.in_scale_row_bytes > 0 && !scales) return fail(EP_ERR_INVALID_ARG, "scale_dim > 0 needs a scales array");
+  if (scales && !aligned(scales, 4)) return fail(EP_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = rank_ready_device(h, st);
+  if (s != EP_OK) return s;
+  h->ntok = num_tokens;
+
+  // routing layout over this rank's tokens: one source, R destinations
+  ep::LayoutParams lp;
+  memset(&lp, 0, sizeof(lp));
+  lp.R = g.R; lp.Tmax = g.Tmax; lp.k = g.k; lp.E_r = g.E_r; lp.E = g.E;
+  lp.cpr = g.cpr; lp.nchunks = g.cpr;
+  lp.ntok[0] = num_tokens;
+  lp.idx = indices;
+  lp.err = h->w.err;
+  lp.mask = h->w.mask;
+  lp.local8 = h->w.local8;
+  lp.recv_num_token = h->w.send_cnt;
+  lp.chunk_cnt = h->w.chunk_cnt;
+  lp.chunk_off = h->w.chunk_off;
+  lp.ticket = h->w.tickets + 0;
+  ep::SplitParams sp;
+  rank_split_params(h, &sp);
+  sp.x = static_cast<const uint8_t*>(x);
+  sp.w = weights;
+  sp.idx = indices;
+  sp.scales_in = static_cast<const uint8_t*>(scales);
+  cudaError_t e = ep::launch_layout_2d(lp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "routing-layout launch");
+  e = ep::launch_split_stage(sp, g.quant ? h->cfg.quant_type : 0, rank_launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch_send launch");
+  h->state = kRSent;
+  fill_rank_dispatch_out(h, out);
+  return EP_OK;
+}
+
+ep_status ep_dispatch_recv(ep_rank_handle* h, void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (h->state != kRSent) return fail(EP_ERR_STATE, "dispatch_recv needs a preceding dispatch_send");
+  if (!h->has_peers) return fail(EP_ERR_STATE, "peer workspaces are not set (ep_rank_set_peers)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = rank_ready_device(h, st);
+  if (s != EP_OK) return s;
+  ep::SplitParams sp;
+  rank_split_params(h, &sp);
+  cudaError_t e = ep::launch_split_pull(sp, rank_peers(h), rank_launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch_recv launch");
+  h->state = kRDispatched;
+  return EP_OK;
+}
+
+ep_status ep_combine_send(ep_rank_handle* h, const void* expert_out, const float* weights,
+                          void* out, float* out_weights, void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (h->state != kRDispatched) return fail(EP_ERR_STATE, "combine_send needs a completed dispatch (send + recv)");
+  if (!out) return fail(EP_ERR_INVALID_ARG, "out must be non-NULL");
+  if (!expert_out) expert_out = h->w.reg_combine_in;  // the experts wrote the registered buffer
+  if (!aligned(expert_out, 16) || !aligned(out, 16))
+    return fail(EP_ERR_INVALID_ARG, "expert_out and out must be 16-byte aligned");
+  if ((h->cfg.weighted_combine || out_weights) && !weights)
+    return fail(EP_ERR_INVALID_ARG, "weighted combine and out_weights need weights");
+  if (weights && !aligned(weights, 4)) return fail(EP_ERR_INVALID_ARG, "weights must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = rank_ready_device(h, st);
+  if (s != EP_OK) return s;
+  const uint8_t* y = static_cast<const uint8_t*>(expert_out);
+  if (y != h->w.reg_combine_in || (weights && weights != h->w.comb_w)) {
+    cudaError_t e = ep::launch_split_copy_rows(y, h->w.reg_combine_in, h->g.combine_in_row_bytes,
+                                               weights, h->w.comb_w, h->g.k, h->w.recv_num_token,
+                                               h->g.cap, rank_launch_cfg(h), st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine_send launch");
+  }
+  h->out = static_cast<uint8_t*>(out);
+  h->out_w = out_weights;
+  h->weighted_w = weights != nullptr;
+  h->state = kRCombineSent;
+  return EP_OK;
+}
+
+ep_status ep_combine_recv(ep_rank_handle* h, int32_t call_reset, void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (h->state != kRCombineSent) return fail(EP_ERR_STATE, "combine_recv needs a preceding combine_send");
+  if (!h->has_peers) return fail(EP_ERR_STATE, "peer workspaces are not set (ep_rank_set_peers)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ep_status s = rank_ready_device(h, st);
+  if (s != EP_OK) return s;
+  const Geometry& g = h->g;
+  ep::CombineParams p;
+  memset(&p, 0, sizeof(p));
+  p.R = g.R; p.Tmax = g.Tmax; p.k = g.k; p.E_r = g.E_r; p.H = g.H;
+  p.ntok[0] = h->ntok;
+  p.cap = g.cap;
+  p.segs_per_token = (g.H + ep::kCombineUnroll * 256 - 1) / (ep::kCombineUnroll * 256);
+  p.total_units = (int64_t)h->ntok * p.segs_per_token;
+  p.weighted = h->cfg.weighted_combine != 0;
+  p.idx = h->w.send_idx;
+  p.out = h->out;
+  p.out_w = h->out_w;
+  p.err = h->w.err;
+  cudaError_t e = ep::launch_split_gather(p, rank_peers(h), h->w.slot_own, h->cfg.combine_dtype,
+                                          h->cfg.combine_out_dtype, rank_launch_cfg(h), st);
+  if (e != cudaSuccess) return cuda_fail(e, "combine_recv launch");
+  h->state = kRCombined;
+  if (call_reset) h->state = kRReady;
+  return EP_OK;
+}
+
+ep_status ep_rank_reset(ep_rank_handle* h) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  h->state = kRReady;
+  return EP_OK;
+}
+
+ep_status ep_rank_get_registered_combine_input_buffer(ep_rank_handle* h, void** d_buffer) {
+  if (!h || !d_buffer) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+  *d_buffer = h->w.reg_combine_in;
+  return EP_OK;
+}
+
+ep_status ep_rank_get_dispatch_src_token_pos(ep_rank_handle* h, const int32_t** d_src_token_pos) {
+  if (!h || !d_src_token_pos) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+  if (h->state == kRReady || h->state == kRSent)
+    return fail(EP_ERR_STATE, "no received rows yet (dispatch_send, then dispatch_recv)");
+  *d_src_token_pos = h->w.src_pos;
+  return EP_OK;
+}
+
+ep_status ep_rank_sync(ep_rank_handle* h, void* stream) {
+  if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (h->needs_init) return EP_OK;
+  int32_t bits = 0;
+  e = cudaMemcpyAsync(&bits, h->w.err, sizeof(bits), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the error flags");
+  if (bits == 0) return EP_OK;
+  e = cudaMemsetAsync(h->w.err, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the error flags");
+  return fail(EP_ERR_INVALID_INDEX, "an expert id was outside [-1, %d)", h->g.E);
+}
+
+}  // extern "C"

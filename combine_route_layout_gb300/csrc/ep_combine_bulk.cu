@@ -27,7 +27,6 @@
 namespace ep {
 namespace {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kCols = 1024;      // columns of one row chunk (one unit)
 constexpr int kStages = 4;       // units in flight per CTA
 constexpr int kRows = 8;         // at most 8 rows per unit

@@ -18,7 +18,6 @@
 namespace ep {
 namespace {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kWarps = kLayoutThreads / 32;
 
 __device__ bool elect_last(unsigned int* ticket) {

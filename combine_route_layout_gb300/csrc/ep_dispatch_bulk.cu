@@ -17,7 +17,6 @@
 namespace ep {
 namespace {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kStages = 4;
 
 struct BulkRing {

@@ -9,7 +9,6 @@
 namespace ep {
 namespace {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Slot of this token on rank `lane` (2D layout), or -1.
 __device__ __forceinline__ int slot_on_lane_rank(const DispatchParams& p, int64_t g, int s, int t,

@@ -142,6 +142,54 @@ struct ConvertParams {
   uint8_t* combine_in;
 };
 
+// Split send / receive phases, one rank per workspace (ep_split.cu).
+struct SplitParams {
+  int R, Tmax, k, E_r, E, H;
+  int ntok;                    // this rank's tokens
+  int64_t cap;                 // receive rows (R * Tmax)
+  int64_t in_row_bytes;        // bytes of one source payload row
+  int64_t out_row_bytes;       // bytes of one staged / received payload row
+  int scale_row_bytes;         // staged / received scale bytes per row (0 = none)
+  int in_scale_row_bytes;      // pass-through input scale bytes per row
+  int segs_per_token;          // stage units per token
+  int segs_per_row;            // pull units per receive row (2 KB each)
+  int64_t total_units;         // stage units
+  // send side (this rank's own memory)
+  const uint8_t* x;
+  const float* w;
+  const int32_t* idx;
+  const uint8_t* scales_in;
+  const uint32_t* mask;        // [Tmax] destination ranks of each own token
+  const uint8_t* local8;       // [Tmax][R]
+  const int32_t* chunk_off;    // [cpr][R]
+  int32_t* slot_own;           // [Tmax][R] position in the list sent to r, or -1
+  int32_t* send_list;          // [R][Tmax] own token ids sent to r, ascending
+  uint8_t* send_x;             // [Tmax][out_row_bytes]
+  uint8_t* send_scales;        // [Tmax][scale_row_bytes]
+  float* send_w;               // [Tmax][k]
+  int32_t* send_idx;           // [Tmax][k]
+  // receive side
+  uint8_t* recv_x;             // [cap][out_row_bytes]
+  uint8_t* recv_scales;
+  float* recv_w;
+  int32_t* recv_idx;
+  int32_t* src_pos;            // [cap]
+  int32_t* recv_off;           // [R] first receive row of each source
+  int32_t* recv_num_token;     // [1]
+  int32_t* err;
+};
+
+// Every rank's workspace base and the byte offsets of the regions peers read
+// (identical on all ranks: same config, same carve).
+struct SplitPeers {
+  const uint8_t* base[EP_MAX_WORLD_SIZE];
+  int rank;
+  int64_t off_send_cnt, off_send_list, off_send_x, off_send_scales, off_send_w, off_send_idx;
+  int64_t off_recv_off;        // receive offsets per source
+  int64_t off_y;               // registered combine input
+  int64_t off_w;               // combine weights in receive layout
+};
+
 // ------------------------------------------------------------------ launchers
 // Each returns the cudaError_t of its launch.
 
@@ -207,6 +255,20 @@ cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
 cudaError_t launch_convert_combine(const ConvertParams& p, int dtype, const LaunchCfg& lc,
                                    cudaStream_t st);
 
+// Split phases (ep_split.cu). quant as for launch_dispatch_2d.
+cudaError_t launch_split_stage(const SplitParams& p, int quant, const LaunchCfg& lc,
+                               cudaStream_t st);
+cudaError_t launch_split_pull(const SplitParams& p, const SplitPeers& pe, const LaunchCfg& lc,
+                              cudaStream_t st);
+// Rows [0, *count) of src into dst (skipped when src == dst) and, when w is
+// given and differs from dst_w, their k weights into dst_w.
+cudaError_t launch_split_copy_rows(const uint8_t* src, uint8_t* dst, int64_t row_bytes,
+                                   const float* w, float* dst_w, int k, const int32_t* count,
+                                   int64_t max_rows, const LaunchCfg& lc, cudaStream_t st);
+cudaError_t launch_split_gather(const CombineParams& p, const SplitPeers& pe,
+                                const int32_t* slot_own, int in_dtype, int out_dtype,
+                                const LaunchCfg& lc, cudaStream_t st);
+
 // Record `msg` as the calling thread's ep_last_error() text; returns `st`.
 ep_status record_error(ep_status st, const char* msg);
 
@@ -242,6 +304,8 @@ inline cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size
 // ---------------------------------------------------------------- device PTX
 #ifdef __CUDACC__
 namespace ep {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;  // every lane of a warp
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 v;

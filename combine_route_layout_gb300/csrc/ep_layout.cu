@@ -22,7 +22,6 @@
 namespace ep {
 namespace {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kWarps = kLayoutThreads / 32;
 
 // Release this CTA's global writes and report whether it finished last.

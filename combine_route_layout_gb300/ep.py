@@ -114,6 +114,18 @@ def _load() -> ctypes.CDLL:
         "ep_set_launch_config": (S, [P, I, I, I, I]),
         "ep_get_launch_config": (S, [P, I, P, P, P]),
         "ep_selftest_bounded_wait": (S, [P, P]),
+        "ep_rank_workspace_size": (Z, [P]),
+        "ep_rank_create": (S, [P, I, P, Z, P]),
+        "ep_rank_destroy": (None, [P]),
+        "ep_rank_set_peers": (S, [P, P]),
+        "ep_dispatch_send": (S, [P, P, P, P, P, I, P, P]),
+        "ep_dispatch_recv": (S, [P, P]),
+        "ep_combine_send": (S, [P, P, P, P, P, P]),
+        "ep_combine_recv": (S, [P, I, P]),
+        "ep_rank_reset": (S, [P]),
+        "ep_rank_get_registered_combine_input_buffer": (S, [P, P]),
+        "ep_rank_get_dispatch_src_token_pos": (S, [P, P]),
+        "ep_rank_sync": (S, [P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -241,6 +253,67 @@ def ep_routing_layout_noalloc(world_size, max_num_inp_token_per_rank, num_expert
                                           num_experts_per_rank, num_experts_per_token, indices,
                                           nt, recv_num_token, src_token_pos, slot_map,
                                           error_flags, stream))
+
+
+# ------------------------------------------- one rank per workspace (split phases)
+
+def ep_rank_workspace_size(cfg: ep_config) -> int:
+    return int(_lib.ep_rank_workspace_size(ctypes.byref(cfg)))
+
+
+def ep_rank_create(cfg: ep_config, rank: int, d_workspace: int, workspace_bytes: int) -> int:
+    h = ctypes.c_void_p()
+    _check(_lib.ep_rank_create(ctypes.byref(cfg), int(rank), d_workspace, workspace_bytes,
+                               ctypes.byref(h)))
+    return h.value
+
+
+def ep_rank_destroy(handle: int) -> None:
+    _lib.ep_rank_destroy(handle)
+
+
+def ep_rank_set_peers(handle, peer_workspaces) -> None:
+    arr = (ctypes.c_void_p * len(peer_workspaces))(*[int(p) for p in peer_workspaces])
+    _check(_lib.ep_rank_set_peers(handle, arr))
+
+
+def ep_dispatch_send(handle, x, weights, scales, indices, num_tokens: int, stream) -> ep_dispatch_out:
+    out = ep_dispatch_out()
+    _check(_lib.ep_dispatch_send(handle, x, weights, scales, indices, int(num_tokens), stream,
+                                 ctypes.byref(out)))
+    return out
+
+
+def ep_dispatch_recv(handle, stream) -> None:
+    _check(_lib.ep_dispatch_recv(handle, stream))
+
+
+def ep_combine_send(handle, expert_out, weights, out, out_weights, stream) -> None:
+    _check(_lib.ep_combine_send(handle, expert_out, weights, out, out_weights, stream))
+
+
+def ep_combine_recv(handle, call_reset, stream) -> None:
+    _check(_lib.ep_combine_recv(handle, int(call_reset), stream))
+
+
+def ep_rank_reset(handle) -> None:
+    _check(_lib.ep_rank_reset(handle))
+
+
+def ep_rank_get_registered_combine_input_buffer(handle) -> int:
+    p = ctypes.c_void_p()
+    _check(_lib.ep_rank_get_registered_combine_input_buffer(handle, ctypes.byref(p)))
+    return p.value
+
+
+def ep_rank_get_dispatch_src_token_pos(handle) -> int:
+    p = ctypes.c_void_p()
+    _check(_lib.ep_rank_get_dispatch_src_token_pos(handle, ctypes.byref(p)))
+    return p.value
+
+
+def ep_rank_sync(handle, stream) -> None:
+    _check(_lib.ep_rank_sync(handle, stream))
 
 
 # ------------------------------------------------------- operator class

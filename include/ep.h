@@ -327,6 +327,121 @@ ep_status ep_sync(ep_handle* h, void* stream);
 const char* ep_last_error(void);
 
 /*
+ * ---------------------------------------------------------------------------
+ * One EP rank per workspace, with split send / receive phases (MORI-EP User
+ * Guide, section 3, "Split dispatch/combine (send + recv)": dispatch_send()
+ * returns the dispatch outputs, dispatch_recv() completes the receive side;
+ * combine_send() returns the combine outputs, combine_recv() completes
+ * them; section 1, the intra-node kernel type, where ranks exchange tokens
+ * over peer-to-peer links).
+ *
+ * Each rank (a process, or a handle in one process) owns one workspace of
+ * ep_rank_workspace_size bytes, created with the same ep_config on every
+ * rank (world_size = number of ranks; standard_moe must be 0). The ranks'
+ * workspaces are carved identically, and each handle is given every rank's
+ * workspace as a device pointer (ep_rank_set_peers): its own, other handles'
+ * in the same process, or peers' memory mapped into this process (CUDA IPC
+ * or fabric handles; the library maps nothing itself). Results equal those
+ * of the single-workspace calls: rank r's receive rows, src_token_pos and
+ * combine outputs are rank r's part of ep_dispatch / ep_combine on the
+ * whole group's inputs.
+ *
+ * Phases. The send calls read and write only the rank's own workspace and
+ * inputs; the receive calls read the peers' workspaces. The caller orders
+ * them: every rank's dispatch_send (and combine_send) must have completed
+ * before any rank's dispatch_recv (combine_recv) starts, and every rank's
+ * dispatch_recv before any rank's next dispatch_send; e.g. each rank
+ * synchronises its stream, then all ranks meet at a host barrier. No kernel
+ * waits on another rank. State per handle: READY -dispatch_send-> SENT
+ * -dispatch_recv-> DISPATCHED -combine_send-> COMBINE_SENT -combine_recv->
+ * COMBINED -ep_rank_reset (or call_reset)-> READY; other orders return
+ * EP_ERR_STATE.
+ * ---------------------------------------------------------------------------
+ */
+typedef struct ep_rank_handle ep_rank_handle;
+
+/* Workspace bytes of one rank for `cfg` (0 if invalid or standard_moe = 1). */
+size_t ep_rank_workspace_size(const ep_config* cfg);
+
+/*
+ * A handle for rank `rank` in [0, world_size) over `d_workspace` (device,
+ * 256-byte aligned, owned by the caller). Makes no CUDA call. With
+ * world_size 1 the handle is its own only peer; otherwise call
+ * ep_rank_set_peers before the first receive phase.
+ */
+ep_status ep_rank_create(const ep_config* cfg, int32_t rank, void* d_workspace,
+                         size_t workspace_bytes, ep_rank_handle** out_handle);
+
+/* Free the host-side handle. NULL is a no-op. */
+void ep_rank_destroy(ep_rank_handle* h);
+
+/*
+ * peer_workspaces: host array [world_size] of device pointers, entry r the
+ * workspace of rank r as this process sees it; entry `rank` must be this
+ * handle's own workspace. State must be READY.
+ */
+ep_status ep_rank_set_peers(ep_rank_handle* h, void* const* peer_workspaces);
+
+/*
+ * dispatch_send(): route this rank's tokens and stage them for the ranks
+ * that own their experts.
+ *   x, weights, scales, indices  device [Tmax][...] of this rank only, as
+ *                                ep_dispatch's inputs for one source rank
+ *   num_tokens                   tokens held by this rank, <= Tmax
+ *   out                          (optional) views of this rank's receive
+ *                                buffers: [cap][...] rows, cap = world_size *
+ *                                Tmax, recv_num_token [1]; valid after
+ *                                dispatch_recv
+ * Each token is read once (and quantised once) into the rank's send buffers.
+ */
+ep_status ep_dispatch_send(ep_rank_handle* h, const void* x, const float* weights,
+                           const void* scales, const int32_t* indices, int32_t num_tokens,
+                           void* stream, ep_dispatch_out* out);
+
+/*
+ * dispatch_recv(): pull this rank's receive rows from every rank's send
+ * buffers, ordered by (source rank, source token), and write recv_num_token
+ * and src_token_pos (src_rank * (world_size * Tmax) + src_token_id).
+ */
+ep_status ep_dispatch_recv(ep_rank_handle* h, void* stream);
+
+/*
+ * combine_send(): expose this rank's expert outputs to the ranks whose
+ * tokens they belong to.
+ *   expert_out   device [cap][H] combine_dtype, rows in receive order; NULL:
+ *                the experts wrote ep_rank_get_registered_combine_input_buffer
+ *   weights      device [cap][k] f32 in receive layout (dispatch's weights
+ *                output or the caller's), or NULL; give weights on every
+ *                rank or on none
+ *   out          device [Tmax][H] combine_out_dtype, this rank's tokens
+ *   out_weights  device [Tmax][k] f32 or NULL (needs weights)
+ * out and out_weights are written by combine_recv.
+ */
+ep_status ep_combine_send(ep_rank_handle* h, const void* expert_out, const float* weights,
+                          void* out, float* out_weights, void* stream);
+
+/*
+ * combine_recv(): for each of this rank's tokens, read its rows from the
+ * ranks holding them and reduce them in ascending rank order, f32 from +0,
+ * weighted as ep_combine; call_reset nonzero: back to READY afterwards.
+ */
+ep_status ep_combine_recv(ep_rank_handle* h, int32_t call_reset, void* stream);
+
+/* reset() for a rank handle: back to READY. Enqueues nothing. */
+ep_status ep_rank_reset(ep_rank_handle* h);
+
+/* Device [cap][H] combine_dtype buffer inside the rank's workspace that peers
+ * read in combine_recv (zero-copy when the experts write it directly). */
+ep_status ep_rank_get_registered_combine_input_buffer(ep_rank_handle* h, void** d_buffer);
+
+/* get_dispatch_src_token_pos() of this rank: device [cap]; after dispatch_recv. */
+ep_status ep_rank_get_dispatch_src_token_pos(ep_rank_handle* h, const int32_t** d_src_token_pos);
+
+/* Wait for `stream`, then report and clear device-detected errors (an expert
+ * id outside [-1, E) in this rank's indices: EP_ERR_INVALID_INDEX). */
+ep_status ep_rank_sync(ep_rank_handle* h, void* stream);
+
+/*
  * Routing layout with no device allocation. The pages have no counterpart:
  * this is the layout half of dispatch on its own, for callers that cannot
  * call cudaMalloc -- plugins and embedded engines whose host application has

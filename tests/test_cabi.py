@@ -173,3 +173,74 @@ def test_launch_config_per_phase(ep):
         assert ep.ep_get_launch_config(h, ep.EP_PHASE_DISPATCH) == (1, -1, 2)
     finally:
         ep.ep_destroy(h)
+
+
+# ------------------------------------------------- one rank per workspace (split phases)
+
+def test_rank_workspace_size(ep):
+    """A rank's workspace holds its own tokens' send buffers and one rank's
+    receive buffers (cap = world_size * Tmax rows), the registered combine
+    input included; the packed layout is not available per rank."""
+    c = small(ep)
+    n = ep.ep_rank_workspace_size(c)
+    assert n >= 8 * 16 * 256 * 2 * 2           # receive payload + registered combine input
+    assert n < ep.ep_workspace_size(c)          # one rank, not the whole group
+    assert ep.ep_rank_workspace_size(small(ep, standard_moe=1)) == 0
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_rank_create(small(ep, standard_moe=1), 0, FAKE, 1 << 30)
+    assert ei.value.status == ep.EP_ERR_UNSUPPORTED
+
+
+def test_rank_create_and_peer_checks(ep):
+    c = small(ep)
+    n = ep.ep_rank_workspace_size(c)
+    for bad in (-1, 8):
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_rank_create(c, bad, FAKE, n)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_rank_create(c, 0, FAKE + 64, n)
+    assert ei.value.status == ep.EP_ERR_WORKSPACE
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_rank_create(c, 0, FAKE, n - 1)
+    assert ei.value.status == ep.EP_ERR_WORKSPACE
+    me = FAKE + 3 * (1 << 32)
+    h = ep.ep_rank_create(c, 3, me, n)
+    try:
+        peers = [FAKE + r * (1 << 32) for r in range(8)]
+        ep.ep_rank_set_peers(h, peers)
+        for broken in ([p + 16 if r == 5 else p for r, p in enumerate(peers)],
+                       [0 if r == 1 else p for r, p in enumerate(peers)],
+                       [p + 256 if r == 3 else p for r, p in enumerate(peers)]):
+            with pytest.raises(ep.EpError) as ei:   # misaligned, NULL, not this rank's own
+                ep.ep_rank_set_peers(h, broken)
+            assert ei.value.status == ep.EP_ERR_INVALID_ARG
+    finally:
+        ep.ep_rank_destroy(h)
+
+
+def test_rank_phase_state_machine_without_device(ep):
+    """READY -send-> SENT -recv-> DISPATCHED -combine_send-> COMBINE_SENT
+    -combine_recv-> COMBINED: every out-of-order call is refused before any
+    launch, and the receive phases need the peer table."""
+    c = small(ep)
+    n = ep.ep_rank_workspace_size(c)
+    h = ep.ep_rank_create(c, 0, FAKE, n)
+    try:
+        for call in (lambda: ep.ep_dispatch_recv(h, None),
+                     lambda: ep.ep_combine_send(h, FAKE, FAKE, FAKE, None, None),
+                     lambda: ep.ep_combine_recv(h, 0, None),
+                     lambda: ep.ep_rank_get_dispatch_src_token_pos(h)):
+            with pytest.raises(ep.EpError) as ei:
+                call()
+            assert ei.value.status == ep.EP_ERR_STATE
+        for args in ((FAKE, FAKE, None, FAKE, 17), (FAKE, FAKE, None, FAKE, -1),
+                     (FAKE + 8, FAKE, None, FAKE, 1), (None, FAKE, None, FAKE, 1)):
+            with pytest.raises(ep.EpError) as ei:
+                ep.ep_dispatch_send(h, *args, None)
+            assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        p = ep.ep_rank_get_registered_combine_input_buffer(h)
+        assert FAKE <= p < FAKE + n and p % 256 == 0
+        ep.ep_rank_reset(h)
+    finally:
+        ep.ep_rank_destroy(h)
