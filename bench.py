@@ -432,17 +432,104 @@ def cpu_oracle_step(wl, tokens_per_rank: int, seed: int = 0, y=None):
     return dt, b["dispatch"] + b["combine"], y
 
 
+def host_cpu():
+    """CPU model, logical CPU count and architecture of the host."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                v = line.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    model = v
+                    break
+    except Exception:
+        pass
+    return {"model": model or platform.processor() or platform.machine(),
+            "nproc": os.cpu_count(), "arch": platform.machine()}
+
+
+class pinned_core:
+    """Run the enclosed CPU work on one core (the first this process may use)."""
+
+    def __enter__(self):
+        self.before = os.sched_getaffinity(0)
+        self.core = min(self.before)
+        os.sched_setaffinity(0, {self.core})
+        return self
+
+    def __exit__(self, *a):
+        os.sched_setaffinity(0, self.before)
+
+
+def pctl(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
 def cpu_baseline(wl, sample_tokens: int, reps: int):
-    dt_tot, by_tot, y = 0.0, 0, None
-    for _ in range(reps):
-        dt, by, y = cpu_oracle_step(wl, sample_tokens, y=y)
-        dt_tot += dt
-        by_tot += by
-    gbs = by_tot / dt_tot / 1e9
+    """The oracle (single-threaded C) on `reps` dispatch + combine passes of the
+    workload restricted to `sample_tokens` tokens per rank, pinned to one core."""
+    dts, bys, y = [], [], None
+    with pinned_core() as pc:
+        for _ in range(reps):
+            dt, by, y = cpu_oracle_step(wl, sample_tokens, y=y)
+            dts.append(dt)
+            bys.append(by)
+    gbs = sum(bys) / sum(dts) / 1e9
+    per = [b / t / 1e9 for b, t in zip(bys, dts)]
+    cpu = host_cpu()
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "pinned_core": pc.core, "cpu_model": cpu["model"], "nproc": cpu["nproc"],
+            "arch": cpu["arch"], "pass_GBps_p10": round(pctl(per, 10), 4),
+            "pass_GBps_p90": round(pctl(per, 90), 4),
             "sample": f"{wl.name} restricted to {sample_tokens} tokens/rank "
                       f"({wl.world_size * sample_tokens} tokens), {reps} dispatch+combine "
-                      f"passes, single-threaded C, {dt_tot:.1f} s"}
+                      f"passes, single-threaded C on one pinned core, {sum(dts):.1f} s"}
+
+
+# tokens/rank of each workload's CPU-oracle sample (about a second or two of C)
+CPU_SAMPLE_TOKENS = {"tiny": 16, "ds_v3_latency": 128, "ds_v3_throughput": 128,
+                     "skewed_zipf_std_moe": 96, "mid_masked": 256, "ds_v3_throughput_fp4": 128}
+ALL_WORKLOADS = ("tiny", "ds_v3_latency", "ds_v3_throughput", "skewed_zipf_std_moe", "mid_masked")
+
+
+def path_dtype(wl) -> str:
+    d = {"fp8": "fp8_e4m3 dispatch (f32 quantisation)",
+         "fp4": "fp4_e2m1 dispatch (f32 quantisation)"}.get(wl.dispatch_dtype, "bf16 dispatch")
+    comb = "weighted " if wl.weighted else ""
+    return f"{d}, bf16 {comb}combine, f32 accumulate, {wl.combine_out_dtype} out"
+
+
+def time_workload(wl, dev, K: int, W: int, cpu_reps: int, with_cpu: bool):
+    """One workload: dispatch and combine µs (median, p10, p90) with CUDA
+    events, GB/s and fraction of the measured HBM peak, plus the oracle's
+    baseline on a sample of the same workload. Inputs of the small workloads
+    fit in L2, so a 256 MB read evicts it before each step (outside the
+    events); the large ones exceed L2."""
+    step = Step(wl, dev)
+    small = step.Ttot * wl.hidden * 2 < 128 * 1024 * 1024
+    flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if small else None
+    _, disp, comb = time_steps(step, K, W, flush, lambda: None)
+    peak, _ = hbm_peak()
+    b = step.bytes
+    rec = {"tokens_per_rank": wl.tokens_per_rank, "world_size": wl.world_size,
+           "hidden": wl.hidden, "topk": wl.topk, "dtype": path_dtype(wl),
+           "standard_moe": wl.standard_moe, "copies_C": step.C, "packed_rows_P": step.P,
+           "kernels": chosen_kernels(step), "iters": K,
+           "l2": "flushed (256 MB read) before each step" if small else "inputs larger than L2"}
+    for name, ts in (("dispatch", disp), ("combine", comb)):
+        us = [t * 1e3 for t in ts]
+        med = statistics.median(us)
+        gbs = b[name] / (med * 1e-6) / 1e9
+        rec[name] = {"us_median": round(med, 2), "us_p10": round(pctl(us, 10), 2),
+                     "us_p90": round(pctl(us, 90), 2), "bytes": b[name], "GBps": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4)}
+    del step, flush
+    torch.cuda.empty_cache()
+    if with_cpu:
+        rec["cpu_baseline"] = cpu_baseline(wl, CPU_SAMPLE_TOKENS.get(wl.name, 64), cpu_reps)
+    return rec
 
 
 # ----------------------------------------------------------- main
@@ -577,24 +664,29 @@ def run_reference(args, wl, rank, world):
     # about two minutes of oracle time at most (~3.5 ms per token/rank per step)
     T = max(8, min(args.ref_tokens, int(120.0 / (0.0035 * (steps + warm)))))
     y = None
-    for _ in range(warm):
-        _, _, y = cpu_oracle_step(wl, T, y=y)
     tot, by = 0.0, 0
-    for _ in range(steps):
-        dt, b, y = cpu_oracle_step(wl, T, y=y)
-        tot += dt
-        by += b
+    with pinned_core() as pc:
+        for _ in range(warm):
+            _, _, y = cpu_oracle_step(wl, T, y=y)
+        for _ in range(steps):
+            dt, b, y = cpu_oracle_step(wl, T, y=y)
+            tot += dt
+            by += b
     gbs = by / tot / 1e9
+    cpu = host_cpu()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
         "ms_per_step": round(tot / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": path_dtype(wl), "data": "synthetic",
         "config": {"workload": wl.name, "sample_tokens_per_rank": T, "world_size": wl.world_size,
                    "experts_per_rank": wl.experts_per_rank, "hidden": wl.hidden, "topk": wl.topk},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "pinned_core": pc.core, "cpu_model": cpu["model"],
+                         "nproc": cpu["nproc"], "arch": cpu["arch"],
                          "sample": f"{wl.name} restricted to {T} tokens/rank per step, "
-                                   f"single-threaded C oracle, {tot:.1f} s over {steps} steps"},
+                                   f"single-threaded C oracle on one pinned core, "
+                                   f"{tot:.1f} s over {steps} steps"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -625,9 +717,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=1024,
-                    help="tokens/rank of the CPU-oracle baseline sample")
-    ap.add_argument("--cpu-reps", type=int, default=4)
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload lines of the other configs")
+    ap.add_argument("--cpu-tokens", type=int, default=256,
+                    help="tokens/rank of the headline workload's CPU-oracle sample")
+    ap.add_argument("--cpu-reps", type=int, default=3)
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="tokens/rank per step of the reference (oracle) arm")
     args = ap.parse_args()
@@ -691,8 +785,8 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": path_dtype(wl), "data": "synthetic",
         "config": {"workload": wl.name, "world_size": wl.world_size,
                    "experts_per_rank": wl.experts_per_rank, "tokens_per_rank": wl.tokens_per_rank,
                    "hidden": wl.hidden, "topk": wl.topk, "dispatch_payload": wl.dispatch_dtype,
@@ -702,9 +796,13 @@ def main():
                    "launch_mode": LAUNCH_MODE, "kernels": chosen_kernels(step),
                    "parallelism": f"replicas x{world}, 8 simulated EP ranks each"},
         "dispatch": {"us_median": round(d_us, 2), "us_mean": round(d_mean, 2),
+                     "us_p10": round(pctl(disp, 10) * 1e3, 2),
+                     "us_p90": round(pctl(disp, 90) * 1e3, 2),
                      "bytes": b["dispatch"], "GBps": round(d_gbs, 1),
                      "frac_of_peak": round(d_gbs / peak, 4)},
         "combine": {"us_median": round(c_us, 2), "us_mean": round(c_mean, 2),
+                    "us_p10": round(pctl(comb, 10) * 1e3, 2),
+                    "us_p90": round(pctl(comb, 90) * 1e3, 2),
                     "bytes": b["combine"], "GBps": round(c_gbs, 1),
                     "frac_of_peak": round(c_gbs / peak, 4)},
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(ach, 1),
@@ -744,6 +842,16 @@ def main():
                        "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                        "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e_ms / ke, 3),
                        "steps": ke}
+    if not args.no_workloads and rank == 0:
+        # every workload of the method's configs, each with its own CPU-oracle
+        # baseline (rank 0 of a single-GPU run only)
+        wk = {}
+        for name in ALL_WORKLOADS:
+            if name == wl.name:
+                continue
+            wk[name] = time_workload(WORKLOADS[name], dev, max(50, min(K, 100)), args.warmup,
+                                     args.cpu_reps, not args.no_cpu_baseline and world == 1)
+        line["workloads"] = wk
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_tokens, args.cpu_reps)
     if rank == 0:
