@@ -2,8 +2,8 @@
 // ring -- same results as combine_2d_kernel / combine_std_kernel, bit for bit.
 //
 // MORI-EP User Guide, section 3, combine() and section 4,
-// combine_standard_moe(); "Choosing an EP API and backend": gather combine in
-// BF16/FP32. A unit is (source token, 1024-column chunk). A CTA takes
+// combine_standard_moe(); "Choosing an EP API and backend" (EP paths table:
+// the combine is a gather, in bf16 or f32). A unit is (source token, 1024-column chunk). A CTA takes
 // whole tokens c, c + G, c + 2G, ... (G CTAs), all chunks of each; or, for
 // small batches, a contiguous balanced range of units over the present
 // tokens (at most one unit more than any other CTA, so a batch of a few

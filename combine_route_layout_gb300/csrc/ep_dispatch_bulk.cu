@@ -46,13 +46,16 @@ __global__ void __launch_bounds__(32) dispatch_bulk_copy_kernel(DispatchParams p
   }
   __syncwarp();
 
-  // prologue: the first kStages rows of this CTA
+  // prologue: the first kStages rows of this CTA. Load j (the CTA's j-th
+  // present token) lands in stage j % kStages, phase (j / kStages) & 1.
+  int issued = 0;
   int64_t load_g = next_present(blockIdx.x);
   for (int s = 0; s < kStages && load_g < ntokens; ++s) {
     if (lane == 0) {
       mbar_arrive_expect_tx(&ring.full[s], rb);
       bulk_g2s(rows + (size_t)s * rb, p.x + load_g * p.in_row_bytes, rb, &ring.full[s]);
     }
+    ++issued;
     load_g = next_present(load_g + gridDim.x);
   }
   pdl_wait();  // the routing layout is complete and visible past this point
@@ -129,14 +132,21 @@ __global__ void __launch_bounds__(32) dispatch_bulk_copy_kernel(DispatchParams p
         bulk_g2s(rows + (size_t)ps * rb, p.x + load_g * p.in_row_bytes, rb, &ring.full[ps]);
       }
     }
+    if (i >= 1 && load_g < ntokens) ++issued;
     if (i >= 1) load_g = __shfl_sync(kFull, load_g < ntokens ? next_present(load_g + gridDim.x)
                                                              : load_g, 0);
   }
   if (lane == 0) {
-    // no copy may still read or write this CTA's shared memory when it exits
+    // no copy may still read or write this CTA's shared memory when it exits:
+    // the stores are drained by the bulk group wait; after a timeout, the
+    // row loads issued for tokens i .. issued-1 are waited for as well (all
+    // of those waits together bounded by about a second)
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     if (!ok) {
-      for (int s = 0; s < kStages; ++s) (void)mbar_try_wait(&ring.full[s], 0);
+      const uint64_t t0 = globaltimer_ns();
+      for (int j = i; j < issued; ++j)
+        while (!mbar_try_wait(&ring.full[j % kStages], (uint32_t)(j / kStages) & 1u))
+          if (globaltimer_ns() - t0 > kMbarWaitNs) break;
     }
   }
 }

@@ -2,7 +2,7 @@
 //
 // MORI-EP User Guide, section 3, dispatch(): each token goes to the ranks that
 // own its top-k experts (owner = expert / num_experts_per_rank, section 2),
-// once per distinct rank (MORI issue 57: "reduce redundant data transfer"),
+// once per distinct rank (MORI issue 57: a token travels to each owning rank once),
 // and dispatch reports recv_num_token. Receive rows are ordered by
 // (source rank, source token), which makes every result deterministic.
 //

@@ -37,7 +37,10 @@ static_assert(kScratchBytes == EP_NOALLOC_SCRATCH_BYTES, "header constant out of
 
 static __device__ __align__(256) unsigned char g_layout_scratch[kScratchBytes];
 
-// Device address of g_layout_scratch per device, looked up once per device.
+// Device address of g_layout_scratch per device: looked up again on every
+// call that is not being captured into a graph (a device reset or another
+// context on the ordinal can move the array), and reused from here while a
+// capture is in progress.
 std::mutex g_mu;
 void* g_scratch_addr[256] = {};
 
@@ -99,22 +102,31 @@ extern "C" ep_status ep_routing_layout_noalloc(int32_t world_size,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 256)
     return noalloc_fail(EP_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess)
+    return noalloc_fail(EP_ERR_CUDA, std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e));
   unsigned char* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-      // Set-up, once per device, with that device current: the host-side name
-      // g_layout_scratch is not a device address; ask the runtime for it.
+    if (cap == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
+      // With this device current: the host-side name g_layout_scratch is not
+      // a device address; ask the runtime for it (the first call on a device
+      // also commits the array under lazy module loading).
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_layout_scratch);
-      if (e != cudaSuccess)
+      if (e == cudaSuccess) {
+        g_scratch_addr[dev] = p;
+      } else if (!g_scratch_addr[dev]) {
         return noalloc_fail(EP_ERR_CUDA,
                             std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-      g_scratch_addr[dev] = p;
+      } else {
+        (void)cudaGetLastError();  // keep the address found by an earlier call
+      }
     }
     base = static_cast<unsigned char*>(g_scratch_addr[dev]);
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // error bits and the last-CTA ticket must start at zero
   e = cudaMemsetAsync(base, 0, kHeader, st);
   if (e != cudaSuccess)

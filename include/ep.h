@@ -20,8 +20,9 @@
  *   section 4 "Standard MoE Compatibility (DeepEP)" (dispatch_standard_moe(),
  *             combine_standard_moe(), convert_dispatch_output(),
  *             convert_combine_input()),
- * and from "Choosing an EP API and backend" (EP paths table: gather combine
- * in BF16/FP32, quantization; restrictions: OCP E4M3 FP8).
+ * and from "Choosing an EP API and backend" (EP paths table: the combine is
+ * a gather, in bf16 or f32, and dispatch may quantise; restrictions: OCP
+ * E4M3 FP8).
  *
  * Thread safety: a handle is not thread-safe; distinct handles are
  * independent. Errors: every call returns an ep_status; ep_last_error()
@@ -204,7 +205,7 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
                       ep_dispatch_out* out);
 
 /*
- * combine() (User Guide, section 3; gather combine): for each source token,
+ * combine() (User Guide, section 3; a gather): for each source token,
  * sum the expert-output rows of its copies in ascending destination-rank
  * order in an f32 accumulator starting at +0, weighted by the rank's slot
  * weights when weighted_combine, and round once to combine_out_dtype.
@@ -460,11 +461,16 @@ ep_status ep_rank_sync(ep_rank_handle* h, void* stream);
  *                   [-1, E) was skipped
  * Results equal those of ep_dispatch (same kernel, same order). Limit:
  * world_size * Tmax <= EP_NOALLOC_MAX_TOKENS, else EP_ERR_INVALID_ARG with a
- * message. The first call on a device looks up the array's device address
- * (once per device, with that device current); make that first call before
- * any stream capture. Every call shares the array and it keeps the last
- * call's contents; each call clears what must start at zero. Calls that
- * overlap on the GPU race on the array: serialise them.
+ * message. Each call looks up the array's device address with its device
+ * current (the first call on a device does this set-up); a call made while
+ * its stream is being captured reuses the address found by an earlier call,
+ * so make the first call before any stream capture. Under CUDA's lazy
+ * module loading (the default) the array is committed on the device by that
+ * first call, so it can need 2.3 MiB of free device memory once: make one
+ * warm-up call before the host application reserves its memory pool; later
+ * calls take no device memory. Every call shares the array and it keeps the
+ * last call's contents; each call clears what must start at zero. Calls
+ * that overlap on the GPU race on the array: serialise them.
  */
 #define EP_NOALLOC_MAX_TOKENS 65536
 #define EP_NOALLOC_SCRATCH_BYTES 2433280

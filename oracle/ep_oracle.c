@@ -17,9 +17,10 @@
  *            3 (Operator API: dispatch(), combine(), reset(),
  *            get_dispatch_src_token_pos()), 4 (Standard MoE Compatibility),
  *            7 (Complete Example).
- *   [Back]   "Choosing an EP API and backend" -- EP paths table (gather
- *            combine in BF16/FP32; quantization), restrictions (OCP E4M3).
- *   [Issue]  MORI issue 57 -- "reduce redundant data transfer".
+ *   [Back]   "Choosing an EP API and backend" -- EP paths table (the
+ *            combine is a gather, in bf16 or f32; dispatch may quantise),
+ *            restrictions (OCP E4M3).
+ *   [Issue]  MORI issue 57 -- a token travels to each owning rank once.
  *   [OCP]    OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding.
  *   [IEEE]   IEEE 754 round-to-nearest-even; bfloat16 = binary32 with the
  *            low 16 significand bits removed.
@@ -284,7 +285,7 @@ void oracle_place_rows(int R, int Tmax, int64_t row_bytes, const int32_t* ntok,
 /* ---------------------------------------------------------------- combine */
 
 /* [Guide] s.3 combine(): gather expert outputs back to the source token;
- * [Back] gather combine in BF16/FP32. y is [R][R*Tmax][H] (y_dtype),
+ * [Back] the combine is a gather, in bf16 or f32. y is [R][R*Tmax][H] (y_dtype),
  * w_recv [R][R*Tmax][k] or NULL, out [R][Tmax][H] (out_dtype),
  * out_w [R][Tmax][k] or NULL. Readings R5, R6. */
 /* One source token g = s*Tmax + t of the 2D combine; out_row [H], out_w_row [k] or NULL. */
@@ -326,7 +327,7 @@ static void combine_token(int R, int Tmax, int k, int E_r, int H, int64_t g, con
 static int64_t dtype_bytes(int dt) { return dt == DT_BF16 ? 2 : 4; }
 
 /* [Guide] s.3 combine(): gather expert outputs back to the source token;
- * [Back] gather combine in BF16/FP32. y is [R][R*Tmax][H] (y_dtype),
+ * [Back] the combine is a gather, in bf16 or f32. y is [R][R*Tmax][H] (y_dtype),
  * w_recv [R][R*Tmax][k] or NULL, out [R][Tmax][H] (out_dtype),
  * out_w [R][Tmax][k] or NULL. Readings R5, R6. */
 int oracle_combine(int R, int Tmax, int k, int E_r, int H, const int32_t* ntok,

@@ -2,8 +2,9 @@
 
 Workload shapes follow the MORI-EP User Guide's DeepSeek-V3 example and
 benchmark tables; the small variants keep several 256-token chunks and a
-ragged tail so every tile path runs. Full-size cases compare all routing
-metadata exactly and payload / combine rows on a seeded sample.
+ragged tail so every tile path runs. The full-size workloads are compared
+whole (every row, scale and token); the forced-kernel variants at full size
+compare all routing metadata and a seeded sample of rows and tokens.
 """
 import json
 
@@ -215,12 +216,16 @@ def test_fp8_passthrough_with_scales():
 
 @pytest.mark.slow
 def test_ds_v3_throughput_full_size():
-    run_2d(WORKLOADS["ds_v3_throughput"], full=False)
+    """The 4096-token DeepSeek-V3 shape whole: every receive row's FP8 codes,
+    block scales, weights and ids, all routing metadata, and every combined
+    token and weight row against the oracle."""
+    run_2d(WORKLOADS["ds_v3_throughput"], full=True)
 
 
 @pytest.mark.slow
 def test_mid_masked_full_size():
-    run_2d(WORKLOADS["mid_masked"], full=False)
+    """The mid-size masked workload whole (every row and token)."""
+    run_2d(WORKLOADS["mid_masked"], full=True)
 
 
 @pytest.mark.slow
@@ -312,7 +317,9 @@ def test_std_variants(over):
 
 @pytest.mark.slow
 def test_skewed_std_full_size():
-    run_std(WORKLOADS["skewed_zipf_std_moe"], full=False)
+    """The Zipf-skewed standard-MoE workload whole: every packed row, the
+    layout, and every token of the weighted f32 combine."""
+    run_std(WORKLOADS["skewed_zipf_std_moe"], full=True)
 
 
 # ------------------------------------------------------------- conversions

@@ -36,28 +36,35 @@ def _via_dispatch(wl, idx_d, ntok):
 
 
 def _via_noalloc(wl, idx_d, ntok):
+    """Run the entry point into outputs allocated beforehand; returns its
+    results and the device memory it took (free memory before minus after)."""
     R, T = wl.world_size, wl.tokens_per_rank
     recv = torch.full((R,), -7, dtype=torch.int32, device="cuda")
     src = torch.full((R, R * T), -7, dtype=torch.int32, device="cuda")
     slot = torch.full((R, T, R), -7, dtype=torch.int32, device="cuda")
     err = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
     E.ep_routing_layout_noalloc(R, T, wl.experts_per_rank, wl.topk, idx_d.data_ptr(),
                                 list(ntok), recv.data_ptr(), src.data_ptr(), slot.data_ptr(),
                                 err.data_ptr(), torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
-    return recv.cpu().numpy(), src.cpu().numpy(), slot.cpu().numpy(), int(err.item())
+    took = free0 - torch.cuda.mem_get_info()[0]
+    return recv.cpu().numpy(), src.cpu().numpy(), slot.cpu().numpy(), int(err.item()), took
 
 
 def test_noalloc_layout_matches_dispatch_on_two_calls():
     cases = [(WORKLOADS["ds_v3_throughput"].with_(hidden=256), 0, False),
              (WORKLOADS["mid_masked"].with_(hidden=256, tokens_per_rank=1500), 1, True)]
-    for wl, seed, ragged in cases:
+    for call, (wl, seed, ragged) in enumerate(cases):
         R, T = wl.world_size, wl.tokens_per_rank
         idx = make_indices(wl, seed)
         ntok = make_num_tokens(wl, ragged=ragged, seed=seed)
         idx_d = torch.from_numpy(idx).cuda()
         recv_ref, src_ref = _via_dispatch(wl, idx_d, ntok)
-        recv, src, slot, err = _via_noalloc(wl, idx_d, ntok)
+        recv, src, slot, err, took = _via_noalloc(wl, idx_d, ntok)
+        if call > 0:   # the first call may commit the static array; later ones take nothing
+            assert took == 0, f"second call took {took} bytes of device memory"
         assert err == 0
         assert np.array_equal(recv, recv_ref)
         for r in range(R):
