@@ -222,7 +222,10 @@ class Step:
             rows = R * T
         self.op.reset()
         self.op.sync()
-        self.y = make_expert_outputs(wl, rows, seed, device=device)
+        if wl.standard_moe:   # expert outputs for every row of the packed pool, [pool, H]
+            self.y = make_expert_outputs(wl.with_(world_size=1), rows, seed, device=device)[0]
+        else:
+            self.y = make_expert_outputs(wl, rows, seed, device=device)
         self.out = torch.empty((R, T, wl.hidden),
                                dtype=torch.float32 if wl.combine_out_dtype == "fp32"
                                else torch.bfloat16, device=device)
@@ -318,11 +321,16 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
     xh = step.x.cpu().pin_memory()
     wh = step.w.cpu().pin_memory()
     ih = step.idx.cpu().pin_memory()
-    # only the expert-output rows the combine reads travel
-    used = step.rank_rows if wl.standard_moe else step.recv
+    # only the expert-output rows the combine reads travel (the packed pool's
+    # ranks are consecutive from row 0)
     yh, ybytes = [], 0
-    for r in range(wl.world_size):
-        n = int(used[r])
+    if wl.standard_moe:
+        n = int(step.rank_rows.sum())
+        h = step.y[:n].cpu().pin_memory()
+        yh.append((None, n, h))
+        ybytes += h.numel() * h.element_size()
+    for r in range(wl.world_size if not wl.standard_moe else 0):
+        n = int(step.recv[r])
         if n == 0:
             continue
         h = step.y[r, :n].cpu().pin_memory()
@@ -359,7 +367,7 @@ def time_e2e(step: Step, K: int, W: int, dist_barrier):
             B["idx"].copy_(ih, non_blocking=True)
         for j, (r, n, h) in enumerate(yh):
             with torch.cuda.stream(up[(j + 1) % len(up)]):
-                B["y"][r, :n].copy_(h, non_blocking=True)
+                (B["y"][:n] if r is None else B["y"][r, :n]).copy_(h, non_blocking=True)
         st.wait_stream(up[0])
         d = step.dispatch(B["x"], B["w"], B["idx"])
         for us in up[1:]:
@@ -576,7 +584,7 @@ def convert_leg(wl, dev, K: int, W: int):
         data_type=torch.bfloat16, world_size=R, hidden_dim=H, scale_dim=0, scale_type_size=4,
         max_token_type_size=4, max_num_inp_token_per_rank=T,
         num_experts_per_rank=wl.experts_per_rank, num_experts_per_token=k,
-        combine_dtype=torch.bfloat16, combine_out_dtype=torch.float32, standard_moe=True)
+        combine_dtype=torch.bfloat16, combine_out_dtype=torch.float32, standard_moe=2)
     op = EpDispatchCombineOp(cfg, dev)
     x = make_tokens(wl, device=dev)
     w = torch.from_numpy(make_weights(wl)).to(dev)

@@ -59,7 +59,7 @@ struct Geometry {
   int R, H, k, E_r, E, Tmax;
   int64_t cap, pcap;
   int cpr, nchunks, cpr_recv, nchunks_recv;
-  bool quant, std_moe, registered_in;
+  bool quant, std_moe, layout2d, registered_in;  // layouts reserved by the config
   int64_t combine_in_row_bytes;
   int64_t in_row_bytes, out_row_bytes;
   int scale_row_bytes;       // received scale row bytes (0 = none)
@@ -87,6 +87,7 @@ struct Carve {
   int32_t* expert_count;
   int32_t* expert_offset;
   int32_t* rank_rows;
+  int32_t* rank_base;
   int64_t* layout_range;
   int32_t* row_map;
   int32_t* packed_src_info;
@@ -112,17 +113,19 @@ Carve carve(const Geometry& g, uint8_t* base) {
   const int64_t R = g.R, T = g.Tmax, k = g.k;
   take(base, off, c.err, 4 * sizeof(int32_t));
   take(base, off, c.tickets, 4 * sizeof(unsigned int));
-  take(base, off, c.mask, R * T * 4);
-  take(base, off, c.local8, R * T * R);
-  take(base, off, c.chunk_cnt2d, (size_t)g.nchunks * R * 4);
-  take(base, off, c.chunk_off2d, (size_t)g.nchunks * R * 4);
-  take(base, off, c.recv_num_token, R * 4);
-  take(base, off, c.slot_map, R * T * R * 4);
-  take(base, off, c.src_pos, R * g.cap * 4);
-  take(base, off, c.recv_x, R * g.cap * g.out_row_bytes);
-  take(base, off, c.recv_scales, R * g.cap * g.scale_row_bytes);
-  take(base, off, c.recv_w, R * g.cap * k * 4);
-  take(base, off, c.recv_idx, R * g.cap * k * 4);
+  if (g.layout2d) {
+    take(base, off, c.mask, R * T * 4);
+    take(base, off, c.local8, R * T * R);
+    take(base, off, c.chunk_cnt2d, (size_t)g.nchunks * R * 4);
+    take(base, off, c.chunk_off2d, (size_t)g.nchunks * R * 4);
+    take(base, off, c.recv_num_token, R * 4);
+    take(base, off, c.slot_map, R * T * R * 4);
+    take(base, off, c.src_pos, R * g.cap * 4);
+    take(base, off, c.recv_x, R * g.cap * g.out_row_bytes);
+    take(base, off, c.recv_scales, R * g.cap * g.scale_row_bytes);
+    take(base, off, c.recv_w, R * g.cap * k * 4);
+    take(base, off, c.recv_idx, R * g.cap * k * 4);
+  }
   if (g.std_moe) {
     take(base, off, c.local16, R * T * k * 2);
     take(base, off, c.chunk_cnt_std, (size_t)g.nchunks * g.E * 4);
@@ -130,11 +133,14 @@ Carve carve(const Geometry& g, uint8_t* base) {
     take(base, off, c.expert_count, (size_t)g.E * 4);
     take(base, off, c.expert_offset, (size_t)g.E * 4);
     take(base, off, c.rank_rows, R * 4);
+    take(base, off, c.rank_base, R * 4);
     take(base, off, c.layout_range, (size_t)g.E * R * 8);
     take(base, off, c.row_map, R * T * k * 4);
-    take(base, off, c.packed_src_info, R * g.pcap * 4);
-    take(base, off, c.packed_x, R * g.pcap * g.out_row_bytes);
-    take(base, off, c.packed_scales, R * g.pcap * g.scale_row_bytes);
+    take(base, off, c.packed_src_info, g.pcap * 4);
+    take(base, off, c.packed_x, g.pcap * g.out_row_bytes);
+    take(base, off, c.packed_scales, g.pcap * g.scale_row_bytes);
+  }
+  if (g.std_moe && g.layout2d) {  // the conversions between the two layouts
     take(base, off, c.conv_local16, R * g.cap * k * 2);
     take(base, off, c.conv_recv_rows, R * g.cap * k * 4);
     take(base, off, c.conv_chunk_cnt, (size_t)g.nchunks_recv * g.E_r * 4);
@@ -189,8 +195,13 @@ ep_status make_geometry(const ep_config* cfg, Geometry* g) {
   x.cpr_recv = (int)((x.cap + ep::kChunk - 1) / ep::kChunk);
   x.nchunks_recv = R * x.cpr_recv;
   x.quant = quant;
+  if (cfg->standard_moe < 0 || cfg->standard_moe > 2)
+    return fail(EP_ERR_INVALID_ARG, "standard_moe must be 0 (2D layout), 1 (packed layout) or 2 (both)");
   x.std_moe = cfg->standard_moe != 0;
+  x.layout2d = cfg->standard_moe != 1;
   x.registered_in = cfg->use_external_inp_buf == 0;
+  if (x.registered_in && !x.layout2d)
+    return fail(EP_ERR_INVALID_ARG, "use_external_inp_buf = 0 needs the 2D layout (standard_moe 0 or 2)");
   x.combine_in_row_bytes = (int64_t)H * dtype_size(cfg->combine_dtype);
   x.in_row_bytes = cfg->data_type == EP_DTYPE_FP4_E2M1X2 ? (int64_t)H / 2 : (int64_t)H * in_sz;
   if (cfg->data_type == EP_DTYPE_FP4_E2M1X2 && H % 32 != 0)
@@ -214,10 +225,12 @@ ep_status make_geometry(const ep_config* cfg, Geometry* g) {
     x.in_scale_row_bytes = x.scale_row_bytes;
   }
   if (x.std_moe) {
-    const int64_t worst = (int64_t)R * T * std::min(k, E_r) + (int64_t)(ep::kPadRows - 1) * E_r;
-    x.pcap = cfg->max_packed_rows_per_rank > 0 ? cfg->max_packed_rows_per_rank : worst;
-    if ((int64_t)R * x.pcap > INT32_MAX)
-      return fail(EP_ERR_INVALID_ARG, "world_size * packed rows per rank exceeds int32");
+    // one pool for all ranks: at most one row per (token, slot), plus at most
+    // 127 padding rows per expert, whatever the routing
+    const int64_t worst = (int64_t)R * T * k + (int64_t)(ep::kPadRows - 1) * R * E_r;
+    x.pcap = cfg->max_packed_rows_per_rank > 0 ? (int64_t)R * cfg->max_packed_rows_per_rank : worst;
+    if (x.pcap > INT32_MAX)
+      return fail(EP_ERR_INVALID_ARG, "packed pool rows exceed int32");
   } else {
     x.pcap = 0;
   }
@@ -445,6 +458,9 @@ ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const v
                       const int32_t* indices, const int32_t* num_tokens, void* stream,
                       ep_dispatch_out* out) {
   if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->g.layout2d)
+    return fail(EP_ERR_INVALID_ARG,
+                "standard_moe = 1 reserves only the packed layout (2 reserves both layouts)");
   if (h->state != kReady) return fail(EP_ERR_STATE, "dispatch needs reset() after the previous iteration");
   ep_status s = check_dispatch_inputs(h, x, weights, scales, indices);
   if (s == EP_OK) s = check_tokens(h, num_tokens);
@@ -595,6 +611,7 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
   lp.expert_count = h->w.expert_count;
   lp.expert_offset = h->w.expert_offset;
   lp.rank_rows = h->w.rank_rows;
+  lp.rank_base = h->w.rank_base;
   lp.layout_range = h->w.layout_range;
   lp.packed_src_info = h->w.packed_src_info;
   lp.pcap = h->g.pcap;
@@ -610,6 +627,7 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
   dp.local16 = h->w.local16;
   dp.chunk_off = h->w.chunk_off_std;
   dp.expert_offset = h->w.expert_offset;
+  dp.rank_base = h->w.rank_base;
   dp.src_pos = h->w.packed_src_info;
   dp.row_map = h->w.row_map;
   dp.out_x = h->w.packed_x;
@@ -632,6 +650,7 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
     out->packed_layout_range = h->w.layout_range;
     out->expert_offset = h->w.expert_offset;
     out->rank_rows = h->w.rank_rows;
+    out->rank_base = h->w.rank_base;
     out->pcap = h->g.pcap;
     out->x_row_bytes = h->g.out_row_bytes;
   }
@@ -665,6 +684,7 @@ ep_status ep_combine_standard_moe(ep_handle* h, const void* expert_out, const fl
   p.y = static_cast<const uint8_t*>(expert_out);
   p.w = weights;
   p.row_map = h->w.row_map;
+  p.rank_base = h->w.rank_base;
   p.out = static_cast<uint8_t*>(out);
   p.err = h->w.err;
   cudaError_t e = use_bulk(h, p, true)
@@ -682,7 +702,8 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
                                      const int32_t* dispatch_indices, void* stream,
                                      ep_std_moe_out* out) {
   if (!h) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
-  if (!h->g.std_moe) return fail(EP_ERR_INVALID_ARG, "config has standard_moe = 0");
+  if (!h->g.std_moe || !h->g.layout2d)
+    return fail(EP_ERR_INVALID_ARG, "the conversions need both layouts (standard_moe = 2)");
   if (!h->has2d || h->state != kDispatched)
     return fail(EP_ERR_STATE, "convert_dispatch_output needs a preceding dispatch");
   if (!dispatch_x || !dispatch_indices)
@@ -715,6 +736,7 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
   p.expert_count = h->w.expert_count;
   p.expert_offset = h->w.expert_offset;
   p.rank_rows = h->w.rank_rows;
+  p.rank_base = h->w.rank_base;
   p.layout_range = h->w.layout_range;
   p.packed_src_info = h->w.packed_src_info;
   p.row_map = h->w.row_map;
@@ -737,6 +759,7 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
     out->packed_layout_range = h->w.layout_range;
     out->expert_offset = h->w.expert_offset;
     out->rank_rows = h->w.rank_rows;
+    out->rank_base = h->w.rank_base;
     out->pcap = g.pcap;
     out->x_row_bytes = g.out_row_bytes;
   }
@@ -836,7 +859,7 @@ ep_status ep_sync(ep_handle* h, void* stream) {
   if (bits & (ep::kErrIndex | ep::kErrDuplicate))
     return fail(EP_ERR_INVALID_INDEX, "an expert id was outside [-1, %d)%s", h->g.E,
                 (bits & ep::kErrDuplicate) ? " or repeated within a token (standard MoE)" : "");
-  return fail(EP_ERR_CAPACITY, "packed rows exceed max_packed_rows_per_rank = %lld",
+  return fail(EP_ERR_CAPACITY, "packed rows exceed the packed pool of %lld rows",
               (long long)h->g.pcap);
 }
 

@@ -69,6 +69,16 @@ __global__ void __launch_bounds__(256) combine_2d_kernel(CombineParams p) {
 template <int IN, int OUT, int MAXD>
 __global__ void __launch_bounds__(256) combine_std_kernel(CombineParams p) {
   constexpr int kSlots = MAXD > 0 ? MAXD : EP_MAX_TOPK;
+  // first pool row of each rank: the owner rank of a pool row is the last
+  // rank whose region starts at or before it
+  __shared__ int base[EP_MAX_WORLD_SIZE];
+  if ((int)threadIdx.x < p.R) base[threadIdx.x] = __ldg(p.rank_base + threadIdx.x);
+  __syncthreads();
+  auto owner = [&](int row) {
+    int r = 0;
+    while (r + 1 < p.R && row >= base[r + 1]) ++r;
+    return r;
+  };
   const int lane = threadIdx.x & 31;
   const int64_t in_row = (int64_t)p.H * dt_size(IN);
   const int64_t out_row = (int64_t)p.H * dt_size(OUT);
@@ -91,7 +101,7 @@ __global__ void __launch_bounds__(256) combine_std_kernel(CombineParams p) {
     if (t >= p.ntok[s]) continue;
 
     const bool valid = row >= 0;
-    const int key = valid ? (int)(row / p.cap) * 32 + lane : 0x7FFFFFFF;
+    const int key = valid ? owner(row) * 32 + lane : 0x7FFFFFFF;
     const float wj = (valid && p.weighted) ? __ldg(p.w + g * p.k + lane) : 0.0f;
     // position of this slot in (owner rank, slot) order
     int pos = 0;

@@ -96,6 +96,10 @@ __global__ void __launch_bounds__(kThreads, 3) combine_bulk_kernel(CombineParams
     }
     mbar_init_fence();
   }
+  // standard MoE: first pool row of each rank (owner of a pool row = the last
+  // rank whose region starts at or before it)
+  __shared__ int base[EP_MAX_WORLD_SIZE];
+  if (STD && (int)threadIdx.x < p.R) base[threadIdx.x] = __ldg(p.rank_base + threadIdx.x);
   __syncthreads();
   const int segs = p.segs_per_token;
   const int64_t T = p.tok_prefix[p.R];   // present tokens
@@ -159,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 3) combine_bulk_kernel(CombineParams
         rmin = m ? __ffs(m) - 1 : 0;
         slmin = __shfl_sync(kFull, sl, rmin);
       } else {
-        const int key = sl >= 0 ? (int)(sl / p.cap) * 32 + lane : 0x7FFFFFFF;
+        int own = 0;
+        while (own + 1 < p.R && sl >= base[own + 1]) ++own;
+        const int key = sl >= 0 ? own * 32 + lane : 0x7FFFFFFF;
         int pos = 0;
         for (int q = 0; q < p.k; ++q) pos += __shfl_sync(kFull, key, q) < key;
         if (sl >= 0) {

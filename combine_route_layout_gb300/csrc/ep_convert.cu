@@ -103,7 +103,16 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
       off += (n + kPadRows - 1) / kPadRows * kPadRows;
     }
     p.rank_rows[rr] = (int32_t)off;
-    if (off > p.pcap) atomicOr(p.err, kErrCapacity);
+  }
+  __syncthreads();
+  // ranks take consecutive regions of the packed pool
+  if (threadIdx.x == 0) {
+    int64_t base = 0;
+    for (int rr = 0; rr < p.R; ++rr) {
+      p.rank_base[rr] = (int32_t)base;
+      base += p.rank_rows[rr];
+    }
+    if (base > p.pcap) atomicOr(p.err, kErrCapacity);
   }
   __syncthreads();
   for (int64_t q = threadIdx.x; q < (int64_t)p.R * p.E_r * kPadRows; q += blockDim.x) {
@@ -111,7 +120,8 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
     const int n = p.expert_count[e];
     const int64_t prow = (int64_t)p.expert_offset[e] + n + pad;
     const int64_t end = (int64_t)p.expert_offset[e] + (n + kPadRows - 1) / kPadRows * kPadRows;
-    if (prow < end && prow < p.pcap) p.packed_src_info[(int64_t)(e / p.E_r) * p.pcap + prow] = -1;
+    const int64_t grow = p.rank_base[e / p.E_r] + prow;
+    if (prow < end && grow < p.pcap) p.packed_src_info[grow] = -1;
   }
   if (threadIdx.x == 0) *p.ticket = 0u;
 }
@@ -144,9 +154,10 @@ __global__ void __launch_bounds__(256) conv_copy_kernel(ConvertParams p) {
       if (e >= 0 && e < E && e / p.E_r == r && l != 0xFFFF) {
         const int el = e % p.E_r;
         const int c = r * p.cpr_recv + (int)(i / kChunk);
-        const int64_t prow = (int64_t)__ldg(p.expert_offset + r * p.E_r + el) +
+        const int64_t prow = (int64_t)__ldg(p.rank_base + r) +
+                             __ldg(p.expert_offset + r * p.E_r + el) +
                              __ldg(p.chunk_off + (int64_t)c * p.E_r + el) + l;
-        if (prow < p.pcap) my_row = (int64_t)r * p.pcap + prow;
+        if (prow < p.pcap) my_row = prow;
       }
     }
     const uint32_t vm = __ballot_sync(kFull, my_row >= 0);
@@ -188,7 +199,7 @@ __global__ void conv_range_kernel(ConvertParams p) {
   const int s = (int)(q % p.R);
   const int e = (int)(q / p.R);  // r * E_r + el
   const int r = e / p.E_r;
-  const int32_t* seg = p.packed_src_info + (int64_t)r * p.pcap + p.expert_offset[e];
+  const int32_t* seg = p.packed_src_info + (int64_t)p.rank_base[r] + p.expert_offset[e];
   const int n = p.expert_count[e];
   auto lower = [&](int64_t key) {
     int lo = 0, hi = n;

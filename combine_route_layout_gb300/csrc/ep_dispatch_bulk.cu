@@ -94,9 +94,10 @@ __global__ void __launch_bounds__(32) dispatch_bulk_copy_kernel(DispatchParams p
         const int l = __ldg(p.local16 + g * p.k + lane);
         if (e >= 0 && e < p.E && l != 0xFFFF) {
           const int c = s * p.cpr + t / kChunk;
-          const int64_t row =
-              (int64_t)__ldg(p.expert_offset + e) + __ldg(p.chunk_off + (int64_t)c * p.E + e) + l;
-          if (row < p.cap) dst_row = (int64_t)(e / p.E_r) * p.cap + row;
+          const int64_t row = (int64_t)__ldg(p.rank_base + e / p.E_r) +
+                              __ldg(p.expert_offset + e) +
+                              __ldg(p.chunk_off + (int64_t)c * p.E + e) + l;
+          if (row < p.cap) dst_row = row;
         }
         p.row_map[g * p.k + lane] = (int32_t)dst_row;
         if (dst_row >= 0) p.src_pos[dst_row] = s * (p.R * p.Tmax) + t;

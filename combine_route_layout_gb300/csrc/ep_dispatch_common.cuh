@@ -33,7 +33,8 @@ __device__ __forceinline__ void recv_from_counts(const DispatchParams& p) {
   p.recv_num_token[threadIdx.x] = n;
 }
 
-// Packed row (global index r*pcap + row) of slot `lane` (standard MoE), or -1.
+// Pool row (rank_base[owner] + row in the owner's region) of slot `lane`
+// (standard MoE), or -1.
 __device__ __forceinline__ int64_t row_on_lane_slot(const DispatchParams& p, int64_t g, int s,
                                                     int t, int lane) {
   if (lane >= p.k) return -1;
@@ -42,10 +43,10 @@ __device__ __forceinline__ int64_t row_on_lane_slot(const DispatchParams& p, int
   const int l = __ldg(p.local16 + g * p.k + lane);
   if (l == 0xFFFF) return -1;
   const int c = s * p.cpr + t / kChunk;
-  const int64_t row =
-      (int64_t)__ldg(p.expert_offset + e) + __ldg(p.chunk_off + (int64_t)c * p.E + e) + l;
+  const int64_t row = (int64_t)__ldg(p.rank_base + e / p.E_r) + __ldg(p.expert_offset + e) +
+                      __ldg(p.chunk_off + (int64_t)c * p.E + e) + l;
   if (row >= p.cap) return -1;  // capacity overflow is flagged by the layout kernel
-  return (int64_t)(e / p.E_r) * p.cap + row;
+  return row;
 }
 
 // Pass-through scale row of token g to receive row `row` (4-byte words when possible).

@@ -36,10 +36,11 @@ struct LayoutParams {
   uint16_t* local16;          // [R*Tmax][k] rank among the chunk's rows of that expert; 0xFFFF = none
   int32_t* expert_count;      // [E]
   int32_t* expert_offset;     // [E] segment start within its rank
-  int32_t* rank_rows;         // [R]
+  int32_t* rank_rows;         // [R] padded rows of each rank
+  int32_t* rank_base;         // [R] first pool row of each rank (prefix of rank_rows)
   int64_t* layout_range;      // [R][E_r][R]
-  int32_t* packed_src_info;   // [R][pcap]
-  int64_t pcap;
+  int32_t* packed_src_info;   // [pool rows]
+  int64_t pcap;               // rows in the packed pool shared by all ranks
   // shared
   int32_t* chunk_cnt;         // [nchunks][R] (2D) or [nchunks][E] (standard MoE)
   int32_t* chunk_off;         // exclusive prefix over chunks, same shape
@@ -51,7 +52,7 @@ struct LayoutParams {
 struct DispatchParams {
   int R, Tmax, k, E_r, E, cpr;
   int ntok[EP_MAX_WORLD_SIZE];
-  int64_t cap;                 // receive rows per rank (2D) or pcap (standard MoE)
+  int64_t cap;                 // receive rows per rank (2D) or packed pool rows (standard MoE)
   int H;
   int64_t in_row_bytes;        // bytes of one source payload row
   int64_t out_row_bytes;       // bytes of one received payload row
@@ -68,9 +69,10 @@ struct DispatchParams {
   const uint16_t* local16;
   const int32_t* chunk_off;
   const int32_t* expert_offset;
+  const int32_t* rank_base;     // standard MoE: first pool row of each rank
   // outputs
   int32_t* slot_map;           // 2D: [R*Tmax][R]
-  int32_t* src_pos;            // 2D: [R][cap]; standard MoE: packed_src_info [R][pcap]
+  int32_t* src_pos;            // 2D: [R][cap]; standard MoE: packed_src_info [pool rows]
   int32_t* row_map;            // standard MoE: [R*Tmax][k] global packed row
   uint8_t* out_x;
   uint8_t* out_scales;         // [rows][H/128] f32 (quant) or [rows][scale_row_bytes]
@@ -98,7 +100,8 @@ struct CombineParams {
   const int32_t* recv_idx;     // 2D: receive-layout expert ids (owner test for weights)
   const int32_t* idx;          // standard MoE: source expert ids
   const int32_t* slot_map;     // 2D
-  const int32_t* row_map;      // standard MoE
+  const int32_t* row_map;      // standard MoE: pool row of each (token, slot)
+  const int32_t* rank_base;    // standard MoE: first pool row of each rank
   uint8_t* out;
   float* out_w;
   int32_t* err;
@@ -110,7 +113,7 @@ struct CombineParams {
 
 struct ConvertParams {
   int R, Tmax, k, E_r;
-  int64_t cap, pcap;
+  int64_t cap, pcap;           // receive rows per rank; packed pool rows
   int cpr_recv;                // chunks per rank over the receive capacity
   int nchunks;
   int H;
@@ -129,6 +132,7 @@ struct ConvertParams {
   int32_t* expert_count;       // [R][E_r]
   int32_t* expert_offset;
   int32_t* rank_rows;
+  int32_t* rank_base;
   int64_t* layout_range;
   int32_t* packed_src_info;
   int32_t* row_map;            // [R*Tmax][k]

@@ -16,7 +16,8 @@
 // The standard-MoE variant (User Guide, section 4) counts rows per expert
 // instead of per rank (no deduplication), using per-warp expert bitmaps in
 // shared memory, and the last CTA also lays out the 128-row padded expert
-// segments and the per-source-rank layout ranges.
+// segments, the per-source-rank layout ranges and each rank's first row in
+// the packed pool the ranks share (the prefix of their padded row counts).
 #include "ep_kernels.cuh"
 
 namespace ep {
@@ -200,7 +201,16 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
       off += (n + kPadRows - 1) / kPadRows * kPadRows;
     }
     p.rank_rows[r] = (int32_t)off;
-    if (off > p.pcap) atomicOr(p.err, kErrCapacity);
+  }
+  __syncthreads();
+  // ranks take consecutive regions of the pool shared by all ranks
+  if (threadIdx.x == 0) {
+    int64_t base = 0;
+    for (int r = 0; r < p.R; ++r) {
+      p.rank_base[r] = (int32_t)base;
+      base += p.rank_rows[r];
+    }
+    if (base > p.pcap) atomicOr(p.err, kErrCapacity);
   }
   __syncthreads();
   // padding rows carry src_info = -1
@@ -209,7 +219,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
     const int n = p.expert_count[e];
     const int64_t row = (int64_t)p.expert_offset[e] + n + q;
     const int64_t end = (int64_t)p.expert_offset[e] + (n + kPadRows - 1) / kPadRows * kPadRows;
-    if (row < end && row < p.pcap) p.packed_src_info[(int64_t)(e / p.E_r) * p.pcap + row] = -1;
+    const int64_t prow = p.rank_base[e / p.E_r] + row;
+    if (row < end && prow < p.pcap) p.packed_src_info[prow] = -1;
   }
   if (threadIdx.x == 0) *p.ticket = 0u;
 }

@@ -84,8 +84,8 @@ class ep_std_moe_out(ctypes.Structure):
     _fields_ = [("packed_x", ctypes.c_void_p), ("packed_scales", ctypes.c_void_p),
                 ("packed_count", ctypes.c_void_p), ("packed_src_info", ctypes.c_void_p),
                 ("packed_layout_range", ctypes.c_void_p), ("expert_offset", ctypes.c_void_p),
-                ("rank_rows", ctypes.c_void_p), ("pcap", ctypes.c_int64),
-                ("x_row_bytes", ctypes.c_int64)]
+                ("rank_rows", ctypes.c_void_p), ("rank_base", ctypes.c_void_p),
+                ("pcap", ctypes.c_int64), ("x_row_bytes", ctypes.c_int64)]
 
 
 def _load() -> ctypes.CDLL:
@@ -337,7 +337,7 @@ class EpDispatchCombineConfig:
     combine_dtype: torch.dtype = torch.bfloat16
     combine_out_dtype: torch.dtype = torch.bfloat16
     weighted_combine: bool = False
-    standard_moe: bool = False
+    standard_moe: bool | int = False    # 0/False: 2D layout; 1/True: packed only; 2: both
     max_packed_rows_per_rank: int = 0
     combine_impl: str = "auto"          # "auto" | "vector" | "bulk"
     dispatch_impl: str = "auto"         # "auto" | "vector" | "bulk" (copy mode)
@@ -559,19 +559,30 @@ class EpDispatchCombineOp:
 
     # section 4 ----------------------------------------------------------------
     def _std_views(self, o: ep_std_moe_out):
+        """Packed layout views. The ranks share one pool of pcap rows: rank r's
+        rows are packed_recv_x[rank_base[r] : rank_base[r] + rank_rows[r]]
+        (device values; `packed_rank_rows` slices them on the host)."""
         cfg = self.config
         R, Er, H = cfg.world_size, cfg.num_experts_per_rank, cfg.hidden_dim
         dt, cols, nsc = self._payload()
         return {
-            "packed_recv_x": self._view(o.packed_x, dt, (R, o.pcap, cols)),
-            "packed_recv_scales": (self._view(o.packed_scales, torch.float32, (R, o.pcap, nsc))
+            "packed_recv_x": self._view(o.packed_x, dt, (o.pcap, cols)),
+            "packed_recv_scales": (self._view(o.packed_scales, torch.float32, (o.pcap, nsc))
                                    if o.packed_scales and nsc is not None else None),
             "packed_recv_count": self._view(o.packed_count, torch.int32, (R, Er)),
-            "packed_recv_src_info": self._view(o.packed_src_info, torch.int32, (R, o.pcap)),
+            "packed_recv_src_info": self._view(o.packed_src_info, torch.int32, (o.pcap,)),
             "packed_recv_layout_range": self._view(o.packed_layout_range, torch.int64, (R, Er, R)),
             "expert_offset": self._view(o.expert_offset, torch.int32, (R, Er)),
             "rank_rows": self._view(o.rank_rows, torch.int32, (R,)),
+            "rank_base": self._view(o.rank_base, torch.int32, (R,)),
         }
+
+    @staticmethod
+    def packed_rank_rows(pool: torch.Tensor, rank_base, rank_rows, r: int) -> torch.Tensor:
+        """Rank r's rows of a packed-pool tensor (host-side bounds: reads the
+        base and row count, so it synchronises with the device)."""
+        b = int(rank_base[r])
+        return pool[b:b + int(rank_rows[r])]
 
     def dispatch_standard_moe(self, input, weights, scales, indices, num_tokens=None,
                               block_num=None, warp_per_block=None):

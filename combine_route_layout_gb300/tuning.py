@@ -153,8 +153,8 @@ def tune_shape(cfg, phase: str, scope: str = "quick", iters: int = 20, seed: int
     # expert outputs: the dispatched rows (any values serve for timing)
     d = run_dispatch()
     if cfg.standard_moe:
-        y = torch.randn((R, d["packed_recv_x"].shape[1], H), generator=g, device=dev,
-                        dtype=cfg.combine_dtype)
+        y = torch.randn((d["packed_recv_x"].shape[0], H), generator=g, device=dev,
+                        dtype=cfg.combine_dtype)   # every row of the packed pool
         n_rows = int((idx >= 0).sum())   # valid (token, slot) pairs; padding rows excluded
     else:
         y = torch.randn((R, op.cap, H), generator=g, device=dev, dtype=cfg.combine_dtype)

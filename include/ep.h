@@ -118,9 +118,14 @@ typedef struct ep_config {
                                             BF16 or FP32 */
     int32_t combine_out_dtype;           /* (+) ep_dtype of combine output: BF16 or FP32 */
     int32_t weighted_combine;            /* (+) 0: plain sum over ranks; 1: weighted sum */
-    int32_t standard_moe;                /* (+) 1: reserve the per-expert packed layout */
-    int32_t max_packed_rows_per_rank;    /* (+) packed rows per rank; 0 = worst case
-                                            R*Tmax*min(k,E_r) + 127*E_r */
+    int32_t standard_moe;                /* (+) layouts the workspace reserves: 0 the 2D
+                                            receive layout; 1 the per-expert packed layout
+                                            only (dispatch_standard_moe /
+                                            combine_standard_moe); 2 both, with the
+                                            conversions between them */
+    int32_t max_packed_rows_per_rank;    /* (+) the packed pool holds world_size times this
+                                            many rows; 0 = the worst case of any routing,
+                                            R*Tmax*k + 127*R*E_r rows in all */
     int32_t block_num;                   /* CTAs per launch; <= 0: one wave sized to the GPU */
     int32_t warp_num_per_block;          /* warps per CTA; <= 0: 8 */
     int32_t combine_impl;                /* (+) ep_combine_impl */
@@ -155,19 +160,26 @@ typedef struct ep_dispatch_out {
  * Standard-MoE (DeepEP-style) packed layout (User Guide, section 4). Rank r
  * holds one contiguous segment per local expert, in ascending expert order,
  * each padded to a multiple of 128 rows; rows inside a segment are ordered
- * by (source rank, source token). Rank r's rows start at r * pcap.
+ * by (source rank, source token). The ranks' regions are consecutive in one
+ * pool of pcap rows: rank r's rows are pool rows rank_base[r] ..
+ * rank_base[r] + rank_rows[r] - 1, rank_base being the exclusive prefix of
+ * rank_rows (device values, written by the dispatch). The pool holds the
+ * worst case of every routing by default: world_size * Tmax * k rows (one
+ * per (token, slot)) plus 127 padding rows per expert.
  */
 typedef struct ep_std_moe_out {
-    void* packed_x;                 /* [R][pcap][H] payload */
-    void* packed_scales;            /* [R][pcap][H/128] (FP8) or [R][pcap][H/32] (FP4) f32
-                                       with quantisation, else NULL */
+    void* packed_x;                 /* [pcap][H] payload (pool) */
+    void* packed_scales;            /* [pcap][H/128] (FP8) or [pcap][H/32] (FP4) f32 with
+                                       quantisation, else NULL */
     int32_t* packed_count;          /* [R][E_r] rows per local expert */
-    int32_t* packed_src_info;       /* [R][pcap] src_token_pos encoding; -1 on padding rows */
+    int32_t* packed_src_info;       /* [pcap] src_token_pos encoding; -1 on padding rows */
     int64_t* packed_layout_range;   /* [R][E_r][R] (begin << 32) | count per source rank,
                                        begin relative to the expert segment */
-    int32_t* expert_offset;         /* [R][E_r] first row of each expert segment */
+    int32_t* expert_offset;         /* [R][E_r] first row of each expert segment within its
+                                       rank's region */
     int32_t* rank_rows;             /* [R] padded rows in use on each rank */
-    int64_t pcap;                   /* rows reserved per rank */
+    int32_t* rank_base;             /* [R] first pool row of each rank's region */
+    int64_t pcap;                   /* rows in the pool */
     int64_t x_row_bytes;
 } ep_std_moe_out;
 
@@ -196,8 +208,9 @@ void ep_destroy(ep_handle* h);
  *              (must be NULL with block quantisation, which computes them)
  *   indices    device [R][Tmax][k] int32 in [-1, R*E_r)
  *   num_tokens host [R], tokens held by each source rank, each <= Tmax
- * Receive rows are ordered by (source rank, source token). State must be
- * READY; afterwards it is DISPATCHED. An out-of-range expert id is skipped
+ * Receive rows are ordered by (source rank, source token). Needs the 2D
+ * layout (standard_moe 0 or 2). State must be READY; afterwards it is
+ * DISPATCHED. An out-of-range expert id is skipped
  * and raises EP_ERR_INVALID_INDEX at the next ep_sync.
  */
 ep_status ep_dispatch(ep_handle* h, const void* x, const float* weights, const void* scales,
@@ -246,7 +259,7 @@ ep_status ep_reset(ep_handle* h, void* stream);
  * dispatch_standard_moe() (User Guide, section 4): routing and copy into
  * the packed per-expert layout in one pass (one row per valid (token, slot),
  * no per-rank deduplication). Same inputs as ep_dispatch. Needs
- * standard_moe = 1. Capacity overflow raises EP_ERR_CAPACITY at ep_sync and
+ * standard_moe = 1 or 2. Capacity overflow raises EP_ERR_CAPACITY at ep_sync and
  * the overflowing rows are not written.
  */
 ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* weights,
@@ -257,7 +270,7 @@ ep_status ep_dispatch_standard_moe(ep_handle* h, const void* x, const float* wei
  * combine_standard_moe() (User Guide, section 4): per source token, over its
  * valid slots in (owner rank, slot) order, acc = fmaf(w, y, acc) (weighted)
  * or acc + y, f32 from +0, rounded once to combine_out_dtype.
- *   expert_out  device [R][pcap][H] combine_dtype, packed layout
+ *   expert_out  device [pcap][H] combine_dtype, in the packed pool's rows
  *   weights     device [R][Tmax][k] f32 source-side router weights (NULL if unweighted)
  *   indices     accepted for API parity; the packed layout is used
  *   out         device [R][Tmax][H]
@@ -273,7 +286,7 @@ ep_status ep_combine_standard_moe(ep_handle* h, const void* expert_out, const fl
  *   dispatch_x        device [R][cap][H] (normally ep_dispatch_out.x)
  *   dispatch_indices  device [R][cap][k] (normally ep_dispatch_out.indices)
  * The result equals ep_dispatch_standard_moe on the same inputs. FP8 scales
- * are carried along when the dispatch quantised.
+ * are carried along when the dispatch quantised. Needs standard_moe = 2.
  */
 ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
                                      const int32_t* dispatch_indices, void* stream,
@@ -284,7 +297,7 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
  * outputs, build the 2D combine input: receive row i of rank r gets the
  * unweighted f32 sum, over the token's slots owned by r in ascending slot
  * order, of their packed rows, rounded once to combine_dtype.
- *   packed_y    device [R][pcap][H] combine_dtype
+ *   packed_y    device [pcap][H] combine_dtype, in the packed pool's rows
  *   combine_in  device [R][cap][H] combine_dtype (rows past recv_num_token untouched)
  * Needs both layouts (ep_dispatch, then ep_convert_dispatch_output).
  */

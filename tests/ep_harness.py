@@ -105,3 +105,37 @@ def sample_tokens(wl, ntok, n, seed=0):
         return g
     pick = np.sort(rng.choice(len(g), size=n, replace=False))
     return np.unique(np.concatenate([g[pick], g[:1], g[-1:]]))
+
+
+# ----------------------------------------------------- standard-MoE packed pool
+
+def std_pcap(wl) -> int:
+    """Per-rank capacity of the oracle's [R][pcap] packed arrays: the worst
+    case of one rank (every token of every rank on all of its experts)."""
+    return wl.world_size * wl.tokens_per_rank * min(wl.topk, wl.experts_per_rank) + \
+        127 * wl.experts_per_rank
+
+
+def std_pool_rows(wl) -> int:
+    """Rows of the library's packed pool by default: one per (token, slot)
+    plus 127 padding rows per expert."""
+    return wl.world_size * wl.tokens_per_rank * wl.topk + 127 * wl.num_experts
+
+
+def pool_to_ranks(pool: np.ndarray, base, rows, pcap: int, fill=0) -> np.ndarray:
+    """A host copy of a packed-pool array [pool rows, ...] rearranged as the
+    oracle's [R][pcap, ...]: rank r's rows base[r] .. base[r] + rows[r] - 1 at
+    the start of its slot, `fill` after them."""
+    R = len(base)
+    out = np.full((R, pcap) + pool.shape[1:], fill, dtype=pool.dtype)
+    for r in range(R):
+        out[r, :rows[r]] = pool[base[r]:base[r] + rows[r]]
+    return out
+
+
+def oracle_rows_to_pool(orow: np.ndarray, base, pcap: int) -> np.ndarray:
+    """The oracle's packed row numbers (r * pcap + row) as pool rows
+    (base[r] + row); -1 stays -1."""
+    orow = np.asarray(orow, np.int64)
+    r, i = orow // pcap, orow % pcap
+    return np.where(orow >= 0, np.asarray(base, np.int64)[np.maximum(r, 0)] + i, -1)

@@ -57,11 +57,18 @@ def cfg(ep, **kw):
 
 
 def test_workspace_size_grows_with_layouts(ep):
+    """standard_moe 0 reserves the 2D receive layout, 1 only the packed pool,
+    2 both (and the conversion scratch)."""
     a = ep.ep_workspace_size(cfg(ep))
-    b = ep.ep_workspace_size(cfg(ep, standard_moe=1))
+    b1 = ep.ep_workspace_size(cfg(ep, standard_moe=1))
+    b2 = ep.ep_workspace_size(cfg(ep, standard_moe=2))
     # 2D receive payload alone: 8 ranks x 32768 rows x 7168 FP8 bytes
     assert a >= 8 * 32768 * 7168
-    assert b > a + 8 * (32768 * 8 + 127 * 32) * 7168 - 1
+    # the packed pool shared by the ranks: one row per (token, slot) plus 127
+    # padding rows per expert, whatever the routing (not 8 per-rank worst cases)
+    pool = 8 * 4096 * 8 + 127 * 256
+    assert pool * 7168 <= b1 < 1.1 * pool * (7168 + 4 * 56 + 4) + 64 * 2**20
+    assert a + pool * 7168 <= b2 < a + b1 + 64 * 2**20
 
 
 @pytest.mark.parametrize("bad", [dict(world_size=0), dict(world_size=33), dict(hidden_dim=100),
@@ -70,7 +77,9 @@ def test_workspace_size_grows_with_layouts(ep):
                                  dict(max_num_inp_token_per_rank=0), dict(data_type=9),
                                  dict(hidden_dim=200), dict(quant_type=5),
                                  dict(combine_out_dtype=2), dict(scale_dim=3),
-                                 dict(data_type=1, quant_type=1), dict(warp_num_per_block=16)])
+                                 dict(data_type=1, quant_type=1), dict(warp_num_per_block=16),
+                                 dict(standard_moe=3), dict(standard_moe=-1),
+                                 dict(standard_moe=1, use_external_inp_buf=0)])
 def test_invalid_configs_rejected(ep, bad):
     c = cfg(ep, **bad)
     assert ep.ep_workspace_size(c) == 0
@@ -143,6 +152,9 @@ def test_state_machine_without_device(ep):
         assert ei.value.status == ep.EP_ERR_INVALID_ARG
         with pytest.raises(ep.EpError) as ei:        # standard_moe = 0
             ep.ep_dispatch_standard_moe(h, FAKE, FAKE, None, FAKE, [1] * 8, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        with pytest.raises(ep.EpError) as ei:        # no packed layout: no conversion
+            ep.ep_convert_dispatch_output(h, FAKE, FAKE, None)
         assert ei.value.status == ep.EP_ERR_INVALID_ARG
         with pytest.raises(ep.EpError) as ei:        # no registered buffer reserved
             ep.ep_get_registered_combine_input_buffer(h)
@@ -244,3 +256,20 @@ def test_rank_phase_state_machine_without_device(ep):
         ep.ep_rank_reset(h)
     finally:
         ep.ep_rank_destroy(h)
+
+
+def test_packed_only_config_refuses_the_2d_calls(ep):
+    """A standard_moe = 1 workspace holds only the packed pool: the 2D
+    dispatch and the conversions are refused before any launch."""
+    c = small(ep, standard_moe=1)
+    h = ep.ep_config_create(c, FAKE, ep.ep_workspace_size(c))
+    try:
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_dispatch(h, FAKE, FAKE, None, FAKE, [1] * 8, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+        assert "packed layout" in ep.ep_last_error()
+        with pytest.raises(ep.EpError) as ei:
+            ep.ep_convert_dispatch_output(h, FAKE, FAKE, None)
+        assert ei.value.status == ep.EP_ERR_INVALID_ARG
+    finally:
+        ep.ep_destroy(h)

@@ -17,7 +17,8 @@ from combine_route_layout_gb300 import EpDispatchCombineOp, EpError
 from combine_route_layout_gb300 import ep as E
 from gen import WORKLOADS, make_expert_outputs
 from ep_harness import (DEV, Inputs, bits16, check_route, host, make_config, oracle_quant,
-                        sample_rows, sample_tokens)
+                        oracle_rows_to_pool, pool_to_ranks, sample_rows, sample_tokens, std_pcap,
+                        std_pool_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -235,9 +236,9 @@ def test_tiny_full_size_seed0():
 
 # ------------------------------------------------------------ standard MoE
 
-def _pcap(wl):
-    return wl.world_size * wl.tokens_per_rank * min(wl.topk, wl.experts_per_rank) + \
-        127 * wl.experts_per_rank
+def _pool_y(wl, rows, seed, dtype=torch.bfloat16):
+    """Stand-in expert outputs for every row of the packed pool, [rows, H]."""
+    return make_expert_outputs(wl.with_(world_size=1), rows, seed, device=DEV, dtype=dtype)[0]
 
 
 def run_std(wl, seed=None, ragged=False, full=True, nsample=256, cfg_over=None):
@@ -248,50 +249,50 @@ def run_std(wl, seed=None, ragged=False, full=True, nsample=256, cfg_over=None):
     R, T, H, Er = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.experts_per_rank
     v = op.dispatch_standard_moe(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
     op.sync()
-    pcap = op.pcap
-    assert pcap == _pcap(wl) or cfg.max_packed_rows_per_rank > 0
+    assert op.pcap == std_pool_rows(wl) or cfg.max_packed_rows_per_rank > 0
+    pcap = std_pcap(wl)                 # the oracle's per-rank capacity
     ref = oracle.std_layout(inp.idx, inp.ntok, Er, pcap)
     assert np.array_equal(host(v["packed_recv_count"]), ref["count"])
     assert np.array_equal(host(v["expert_offset"]), ref["seg_off"])
     assert np.array_equal(host(v["rank_rows"]), ref["rank_rows"])
     assert np.array_equal(host(v["packed_recv_layout_range"]), ref["layout_range"])
+    base = host(v["rank_base"]).astype(np.int64)
+    assert np.array_equal(base, np.concatenate([[0], np.cumsum(ref["rank_rows"])[:-1]]))
     gsi = host(v["packed_recv_src_info"])
     for r in range(R):
         n = ref["rank_rows"][r]
-        assert np.array_equal(gsi[r, :n], ref["src_info"][r, :n]), f"src_info rank {r}"
+        assert np.array_equal(gsi[base[r]:base[r] + n], ref["src_info"][r, :n]), f"src_info rank {r}"
     quant = cfg.quant_type != "none"
     data = [(r, i) for r in range(R) for i in np.nonzero(ref["src_info"][r] >= 0)[0]]
     if not full:
         rng = np.random.default_rng(1)
         data = [data[j] for j in np.sort(rng.choice(len(data), size=min(len(data), 8 * nsample),
                                                     replace=False))]
-    rr = np.array([r for r, _ in data])
-    ii = np.array([i for _, i in data])
+    gi = torch.as_tensor(np.array([base[r] + i for r, i in data], np.int64), device=DEV)
     st = np.array([divmod(int(ref["src_info"][r, i]), R * T) for r, i in data])
     xb = inp.x_bits((st[:, 0], st[:, 1]))
-    gx = host(v["packed_recv_x"][torch.as_tensor(rr, device=DEV), torch.as_tensor(ii, device=DEV)])
+    gx = host(v["packed_recv_x"][gi])
     if quant:
         q, sc = oracle_quant(cfg, xb)
-        gsc = host(v["packed_recv_scales"][torch.as_tensor(rr, device=DEV),
-                                           torch.as_tensor(ii, device=DEV)])
+        gsc = host(v["packed_recv_scales"][gi])
         assert np.array_equal(gx, q)
         assert np.array_equal(gsc.view(np.uint32), sc.view(np.uint32))
     else:
         assert np.array_equal(gx, xb), "packed payload"
 
-    # combine_standard_moe on random packed expert outputs
-    Y = make_expert_outputs(wl, pcap, seed, device=DEV, dtype=cfg.combine_dtype)
+    # combine_standard_moe on random expert outputs over the whole pool
+    Y = _pool_y(wl, op.pcap, seed, dtype=cfg.combine_dtype)
     out_d = op.combine_standard_moe(Y, inp.w_d, inp.idx_d, call_reset=True)
     op.sync()
     od = "fp32" if cfg.combine_out_dtype == torch.float32 else "bf16"
     toks = (np.array([s * T + t for s in range(R) for t in range(int(inp.ntok[s]))], np.int64)
             if full else sample_tokens(wl, inp.ntok, 4 * nsample))
-    # gather the rows the sampled tokens use (oracle layout) into a compact Y
+    # gather the rows the tokens use (oracle layout) into a compact Y
     rm = ref["row_map"].reshape(-1, wl.topk)[toks]
     used = np.unique(rm[rm >= 0])
     remap = np.full(R * pcap, -1, np.int64)
     remap[used] = np.arange(len(used))
-    Ysub = host(Y.view(R * pcap, H)[torch.as_tensor(used, device=DEV)])
+    Ysub = host(Y[torch.as_tensor(oracle_rows_to_pool(used, base, pcap), device=DEV)])
     rm_sub = np.full((R * T, wl.topk), -1, np.int32)
     rm_sub[toks] = np.where(rm >= 0, remap[np.maximum(rm, 0)], -1)
     out_ref = oracle.std_combine_tokens(toks, Ysub, inp.idx, rm_sub.reshape(R, T, wl.topk), Er,
@@ -328,18 +329,20 @@ def test_convert_round_trip():
     wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=260, hidden=1024, mask_prob=0.1)
     R, T, H, Er, k = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.experts_per_rank, wl.topk
     inp = Inputs(wl, 3, ragged=True)
-    cfg = make_config(wl, standard_moe=True, combine_dtype=torch.bfloat16,
+    cfg = make_config(wl, standard_moe=2, combine_dtype=torch.bfloat16,
                       combine_out_dtype=torch.float32, weighted_combine=False)
     op = EpDispatchCombineOp(cfg)
     d_x, d_w, _, d_idx, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
     px, pcount, psrc, prange = op.convert_dispatch_output(d_x, d_idx)
     op.sync()
-    pcap = op.pcap
+    assert op.pcap == std_pool_rows(wl)
+    pcap = std_pcap(wl)
     ref = oracle.std_dispatch(inp.x_bits(), inp.idx, inp.ntok, Er, pcap)
     assert np.array_equal(host(pcount), ref["count"])
     assert np.array_equal(host(prange), ref["layout_range"])
-    gsi = host(psrc)
-    gx = host(px)
+    base = np.concatenate([[0], np.cumsum(ref["rank_rows"])[:-1]]).astype(np.int64)
+    gsi = pool_to_ranks(host(psrc), base, ref["rank_rows"], pcap, fill=-2)
+    gx = pool_to_ranks(host(px), base, ref["rank_rows"], pcap)
     for r in range(R):
         n = ref["rank_rows"][r]
         assert np.array_equal(gsi[r, :n], ref["src_info"][r, :n])
@@ -347,9 +350,9 @@ def test_convert_round_trip():
         assert np.array_equal(gx[r, :n][used], ref["x"][r, :n][used])
 
     recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, Er)
-    Y = make_expert_outputs(wl, pcap, 3, device=DEV)
+    Y = _pool_y(wl, op.pcap, 3)
     y2d = op.convert_combine_input(Y, psrc, prange)
-    Yh = host(Y)
+    Yh = pool_to_ranks(host(Y), base, ref["rank_rows"], pcap)
     y2d_ref = oracle.convert_combine_input(Yh, recv, src_pos, inp.idx, ref["row_map"], Er,
                                            out_dtype="bf16")
     gy = host(y2d)
@@ -898,7 +901,7 @@ def test_convert_dispatch_output_carries_quantised_rows(quant):
                                                dispatch_dtype=quant)
     R, T, Er = wl.world_size, wl.tokens_per_rank, wl.experts_per_rank
     inp = Inputs(wl, 5, ragged=True)
-    cfg = make_config(wl, standard_moe=True)
+    cfg = make_config(wl, standard_moe=2)
     op = EpDispatchCombineOp(cfg)
     d_x, d_w, d_sc, d_idx, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
     o = E.ep_convert_dispatch_output(op._handle, d_x.data_ptr(), d_idx.data_ptr(),
@@ -906,10 +909,14 @@ def test_convert_dispatch_output_carries_quantised_rows(quant):
     v = op._std_views(o)
     op.sync()
     q, sc = oracle_quant(cfg, inp.x_bits())
-    ref = oracle.std_layout(inp.idx, inp.ntok, Er, o.pcap)
-    px_ref = oracle.std_place_rows(q, inp.ntok, ref["row_map"], o.pcap)
-    ps_ref = oracle.std_place_rows(sc, inp.ntok, ref["row_map"], o.pcap)
-    gx, gs, gsi = host(v["packed_recv_x"]), host(v["packed_recv_scales"]), host(v["packed_recv_src_info"])
+    pcap = std_pcap(wl)
+    ref = oracle.std_layout(inp.idx, inp.ntok, Er, pcap)
+    px_ref = oracle.std_place_rows(q, inp.ntok, ref["row_map"], pcap)
+    ps_ref = oracle.std_place_rows(sc, inp.ntok, ref["row_map"], pcap)
+    base, rows = host(v["rank_base"]).astype(np.int64), ref["rank_rows"]
+    gx = pool_to_ranks(host(v["packed_recv_x"]), base, rows, pcap)
+    gs = pool_to_ranks(host(v["packed_recv_scales"]), base, rows, pcap)
+    gsi = pool_to_ranks(host(v["packed_recv_src_info"]), base, rows, pcap, fill=-2)
     for r in range(R):
         n = ref["rank_rows"][r]
         used = ref["src_info"][r, :n] >= 0
