@@ -76,19 +76,18 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel_key: str, workload: str | None = None):
-    """Per-launch DRAM bytes from a committed ncu summary, if the kernel
-    source has not changed since it was captured (and, when given, the
-    summary is of this workload)."""
+def profiled_traffic(kernel_key: str, workload: str):
+    """Per-launch DRAM bytes from a committed one-pass ncu capture of this
+    phase's kernel on this workload (profiles/traffic.json), if none of the
+    kernel's source files has changed since it was captured."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            rec = json.load(f)[kernel_key]
-        if workload is not None and rec["workload"].split()[0] != workload:
-            return None
-        src = os.path.join(ROOT, rec["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != rec["source_sha256_16"]:
+            rec = json.load(f)[f"{kernel_key}:{workload}"]
+        m = hashlib.sha256()
+        for src in rec["sources"]:
+            m.update(open(os.path.join(ROOT, src), "rb").read())
+        if m.hexdigest()[:16] != rec["sources_sha256_16"]:
             return None
         return rec
     except Exception:
@@ -526,6 +525,7 @@ def time_workload(wl, dev, K: int, W: int, cpu_reps: int, with_cpu: bool):
            "standard_moe": wl.standard_moe, "copies_C": step.C, "packed_rows_P": step.P,
            "kernels": chosen_kernels(step), "iters": K,
            "l2": "flushed (256 MB read) before each step" if small else "inputs larger than L2"}
+    kern = chosen_kernels(step)
     for name, ts in (("dispatch", disp), ("combine", comb)):
         us = [t * 1e3 for t in ts]
         med = statistics.median(us)
@@ -533,6 +533,9 @@ def time_workload(wl, dev, K: int, W: int, cpu_reps: int, with_cpu: bool):
         rec[name] = {"us_median": round(med, 2), "us_p10": round(pctl(us, 10), 2),
                      "us_p90": round(pctl(us, 90), 2), "bytes": b[name], "GBps": round(gbs, 1),
                      "frac_of_peak": round(gbs / peak, 4)}
+        tr = profiled_traffic(f"{name}_{'std' if wl.standard_moe else '2d'}", wl.name)
+        rec[name]["traffic"] = (tr["dram_bytes_per_launch"]
+                                if tr and tr["kernel"].startswith(kern[name]) else None)
     del step, flush
     torch.cuda.empty_cache()
     if with_cpu:
@@ -631,6 +634,85 @@ def convert_leg(wl, dev, K: int, W: int):
     return out
 
 
+def split_leg(wl, dev, K: int, W: int):
+    """The split send / receive phases with every rank a handle on this GPU
+    (User Guide, section 3, split dispatch/combine): dispatch = every rank's
+    dispatch_send, then every rank's dispatch_recv; combine = every rank's
+    combine_send, then every rank's combine_recv; one stream orders the
+    phases. Bytes as for the single-workspace path (the same receive rows and
+    outputs), so GB/s compare directly; the send phase's staging is extra."""
+    from combine_route_layout_gb300 import EpDispatchCombineConfig
+    from combine_route_layout_gb300.ranks import EpRankOp
+    R, T = wl.world_size, wl.tokens_per_rank
+    cfg = EpDispatchCombineConfig(
+        data_type=torch.bfloat16, world_size=R, hidden_dim=wl.hidden, scale_dim=0,
+        scale_type_size=4, max_token_type_size=4, max_num_inp_token_per_rank=T,
+        num_experts_per_rank=wl.experts_per_rank, num_experts_per_token=wl.topk,
+        quant_type={"fp8": "fp8_e4m3_block128", "fp4": "fp4_e2m1_block32"}.get(wl.dispatch_dtype,
+                                                                            "none"),
+        combine_dtype=torch.bfloat16,
+        combine_out_dtype=torch.float32 if wl.combine_out_dtype == "fp32" else torch.bfloat16,
+        weighted_combine=wl.weighted)
+    ops = [EpRankOp(cfg, r, dev) for r in range(R)]
+    ptrs = [op.workspace.data_ptr() for op in ops]
+    for op in ops:
+        op.set_peers(ptrs)
+    x = make_tokens(wl, 0, device=dev)
+    idx = torch.from_numpy(make_indices(wl, 0)).to(dev)
+    w = torch.from_numpy(make_weights(wl, 0)).to(dev)
+    ntok = make_num_tokens(wl)
+    y = make_expert_outputs(wl, R * T, 0, device=dev)
+    outs = [torch.empty((T, wl.hidden), dtype=cfg.combine_out_dtype, device=dev) for _ in range(R)]
+
+    def dispatch():
+        views = [op.dispatch_send(x[r], w[r], None, idx[r], int(ntok[r]))
+                 for r, op in enumerate(ops)]
+        for op in ops:
+            op.dispatch_recv()
+        return views
+
+    def combine(views):
+        for r, op in enumerate(ops):
+            op.combine_send(y[r], views[r][1] if wl.weighted else None, out=outs[r],
+                            want_weights=False)
+        for op in ops:
+            op.combine_recv(call_reset=True)
+
+    views = dispatch()
+    torch.cuda.synchronize()
+    recv = torch.cat([v[4] for v in views]).cpu().numpy()
+    combine(views)
+    b = algorithmic_bytes(wl, int(recv.sum()), 0, int(ntok.sum()))
+    small = int(ntok.sum()) * wl.hidden * 2 < 128 * 1024 * 1024
+    flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if small else None
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    d_us, c_us = [], []
+    for it in range(W + K):
+        if flush is not None:
+            torch.sum(flush, dim=0, out=sink)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(st)
+        views = dispatch()
+        e[1].record(st)
+        combine(views)
+        e[2].record(st)
+        torch.cuda.synchronize()
+        if it >= W:
+            d_us.append(e[0].elapsed_time(e[1]) * 1e3)
+            c_us.append(e[1].elapsed_time(e[2]) * 1e3)
+    peak, _ = hbm_peak()
+    rec = {"workload": wl.name, "ranks": R, "iters": K,
+           "l2": "flushed (256 MB read) before each step" if small else "inputs larger than L2"}
+    for name, us in (("dispatch", d_us), ("combine", c_us)):
+        med = statistics.median(us)
+        gbs = b[name] / (med * 1e-6) / 1e9
+        rec[name] = {"us_median": round(med, 2), "us_p10": round(pctl(us, 10), 2),
+                     "us_p90": round(pctl(us, 90), 2), "GBps": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4)}
+    return rec
+
+
 def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -718,6 +800,8 @@ def main():
     ap.add_argument("--dispatch-impl", default="auto", choices=["auto", "vector", "bulk"])
     ap.add_argument("--sweep", action="store_true",
                     help="time dispatch/combine over launch configurations instead")
+    ap.add_argument("--split", action="store_true",
+                    help="time the split send/receive phases (every rank a handle) instead")
     ap.add_argument("--e2e-streams", type=int, default=2,
                     help="side streams carrying the expert-output H2D copies in the e2e leg")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
@@ -760,6 +844,11 @@ def main():
         if rank == 0:
             print(json.dumps(sweep(wl, dev, args.steps, args.warmup)), flush=True)
         return
+    if args.split:
+        if rank == 0:
+            print(json.dumps({"split_path": split_leg(wl, dev, args.steps, args.warmup)}),
+                  flush=True)
+        return
     if args.convert:
         if rank == 0:
             print(json.dumps({"convert_path": convert_leg(wl, dev, args.steps, args.warmup)}),
@@ -788,7 +877,7 @@ def main():
     dom_kernel = chosen_kernels(step)[dom]
     ach = c_gbs if dom == "combine" else d_gbs
     tr = profiled_traffic(dom_key, wl.name)
-    if tr and not tr["kernel"].startswith(dom_kernel.replace("_kernel", "")):
+    if tr and not tr["kernel"].startswith(dom_kernel):
         tr = None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
