@@ -13,6 +13,8 @@
 //
 // convert_combine_input: receive row i of rank r becomes the unweighted f32
 // sum of the token's packed rows on r (slots ascending), rounded once.
+#include <algorithm>
+
 #include "ep_kernels.cuh"
 
 namespace ep {
@@ -83,51 +85,71 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
   }
 
   if (!elect_last(p.ticket)) return;
+  // Last CTA: per (rank, local expert), scan its counts over the rank's
+  // receive-row chunks, 16 loads in flight per thread; then the padded
+  // segments, each rank's first pool row and the padding rows, with the
+  // counts and offsets kept in shared memory (the bitmaps are done).
+  int* s_cnt = reinterpret_cast<int*>(dyn);         // [R * E_r]
+  int* s_off = s_cnt + p.R * p.E_r;                  // [R * E_r]
+  __shared__ int s_base[EP_MAX_WORLD_SIZE];
+  __syncthreads();
   for (int q = threadIdx.x; q < p.R * p.E_r; q += blockDim.x) {
     const int rr = q / p.E_r, el = q % p.E_r;
     int run = 0;
-    for (int cc = 0; cc < p.cpr_recv; ++cc) {
-      const int64_t ci = (int64_t)(rr * p.cpr_recv + cc) * p.E_r + el;
-      const int v = __ldcg(p.chunk_cnt + ci);
-      p.chunk_off[ci] = run;
-      run += v;
+    for (int c0 = 0; c0 < p.cpr_recv; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = c0 + j < p.cpr_recv
+                   ? __ldcg(p.chunk_cnt + (int64_t)(rr * p.cpr_recv + c0 + j) * p.E_r + el)
+                   : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c0 + j >= p.cpr_recv) break;
+        p.chunk_off[(int64_t)(rr * p.cpr_recv + c0 + j) * p.E_r + el] = run;
+        run += v[j];
+      }
     }
     p.expert_count[q] = run;
+    s_cnt[q] = run;
   }
   __syncthreads();
   for (int rr = threadIdx.x; rr < p.R; rr += blockDim.x) {
-    int64_t off = 0;
+    int off = 0;
     for (int el = 0; el < p.E_r; ++el) {
-      p.expert_offset[rr * p.E_r + el] = (int32_t)off;
-      const int64_t n = p.expert_count[rr * p.E_r + el];
-      off += (n + kPadRows - 1) / kPadRows * kPadRows;
+      const int q = rr * p.E_r + el;
+      p.expert_offset[q] = off;
+      s_off[q] = off;
+      off += (s_cnt[q] + kPadRows - 1) / kPadRows * kPadRows;
     }
-    p.rank_rows[rr] = (int32_t)off;
+    p.rank_rows[rr] = off;
+    s_base[rr] = off;
   }
   __syncthreads();
   // ranks take consecutive regions of the packed pool
   if (threadIdx.x == 0) {
     int64_t base = 0;
     for (int rr = 0; rr < p.R; ++rr) {
+      const int rows = s_base[rr];
+      s_base[rr] = (int)base;
       p.rank_base[rr] = (int32_t)base;
-      base += p.rank_rows[rr];
+      base += rows;
     }
     if (base > p.pcap) atomicOr(p.err, kErrCapacity);
   }
   __syncthreads();
-  for (int64_t q = threadIdx.x; q < (int64_t)p.R * p.E_r * kPadRows; q += blockDim.x) {
-    const int e = (int)(q / kPadRows), pad = (int)(q % kPadRows);
-    const int n = p.expert_count[e];
-    const int64_t prow = (int64_t)p.expert_offset[e] + n + pad;
-    const int64_t end = (int64_t)p.expert_offset[e] + (n + kPadRows - 1) / kPadRows * kPadRows;
-    const int64_t grow = p.rank_base[e / p.E_r] + prow;
-    if (prow < end && grow < p.pcap) p.packed_src_info[grow] = -1;
+  for (int q = warp; q < p.R * p.E_r; q += kWarps) {  // one warp per expert
+    const int n = s_cnt[q];
+    const int npad = (n + kPadRows - 1) / kPadRows * kPadRows - n;
+    const int64_t row0 = (int64_t)s_base[q / p.E_r] + s_off[q] + n;
+    for (int j = lane; j < npad; j += 32)
+      if (row0 + j < p.pcap) p.packed_src_info[row0 + j] = -1;
   }
   if (threadIdx.x == 0) *p.ticket = 0u;
 }
 
 template <bool SCALES>
-__global__ void __launch_bounds__(256) conv_copy_kernel(ConvertParams p) {
+__global__ void __launch_bounds__(256, 4) conv_copy_kernel(ConvertParams p) {
   const int lane = threadIdx.x & 31;
   const int E = p.R * p.E_r;
   const int64_t stride = (int64_t)p.R * p.Tmax;  // src_token_pos rank stride
@@ -276,7 +298,11 @@ __global__ void __launch_bounds__(256) conv_combine_kernel(ConvertParams p) {
 cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
                                     const LaunchCfg& lc, cudaStream_t st) {
   if (p.nchunks == 0) return cudaSuccess;
-  const size_t smem = (size_t)kWarps * p.E_r * (sizeof(uint32_t) + 1);
+  // per-warp bitmaps and prefixes, reused by the last CTA for two int arrays
+  // of R * E_r
+  const size_t smem = std::max((size_t)kWarps * p.E_r * (sizeof(uint32_t) + 1),
+                               (size_t)p.R * p.E_r * 2 * sizeof(int));
+  if (smem > 48 * 1024) (void)ctas_per_sm(conv_layout_kernel, kLayoutThreads, smem);
   conv_layout_kernel<<<p.nchunks, kLayoutThreads, smem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -167,60 +167,74 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
   }
 
   if (!elect_last_cta(p.ticket)) return;
-  // Last CTA: per expert, scan over chunks (grouped by source rank), then the
-  // padded segment offsets per destination rank and the padding rows.
+  // Last CTA: per expert, scan its counts over the chunks in (source rank,
+  // chunk) order, 16 loads in flight per thread; then the padded segment
+  // offsets per destination rank, each rank's first pool row, and the
+  // padding rows. The counts and offsets stay in shared memory (the expert
+  // bitmaps are no longer needed) for the later passes.
+  int* s_cnt = reinterpret_cast<int*>(dyn);         // [E]
+  int* s_off = s_cnt + p.E;                          // [E]
+  __shared__ int s_base[EP_MAX_WORLD_SIZE];
+  __syncthreads();                                   // every warp is done with the bitmaps
   const int32_t* __restrict__ cnt = p.chunk_cnt;
   int32_t* __restrict__ coff = p.chunk_off;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     const int r = e / p.E_r, el = e % p.E_r;
-    int run = 0;
-    for (int src = 0; src < p.R; ++src) {
-      const int begin = run;
-      for (int cc0 = 0; cc0 < p.cpr; cc0 += 8) {   // 8 independent loads, then the stores
-        int v[8];
+    int run = 0, begin = 0, src = 0, cc = 0;       // chunk c = src * cpr + cc
+    for (int c0 = 0; c0 < p.nchunks; c0 += 16) {
+      int v[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          v[q] = cc0 + q < p.cpr ? __ldcg(cnt + (int64_t)(src * p.cpr + cc0 + q) * p.E + e) : 0;
+      for (int q = 0; q < 16; ++q)
+        v[q] = c0 + q < p.nchunks ? __ldcg(cnt + (int64_t)(c0 + q) * p.E + e) : 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (cc0 + q < p.cpr) coff[(int64_t)(src * p.cpr + cc0 + q) * p.E + e] = run;
-          run += v[q];
+      for (int q = 0; q < 16; ++q) {
+        if (c0 + q >= p.nchunks) break;
+        if (cc == 0) begin = run;
+        coff[(int64_t)(c0 + q) * p.E + e] = run;
+        run += v[q];
+        if (++cc == p.cpr) {  // last chunk of source rank `src`
+          p.layout_range[((int64_t)r * p.E_r + el) * p.R + src] =
+              (int64_t)(((uint64_t)(uint32_t)begin << 32) | (uint32_t)(run - begin));
+          cc = 0;
+          ++src;
         }
       }
-      p.layout_range[((int64_t)r * p.E_r + el) * p.R + src] =
-          (int64_t)(((uint64_t)(uint32_t)begin << 32) | (uint32_t)(run - begin));
     }
     p.expert_count[e] = run;
+    s_cnt[e] = run;
   }
   __syncthreads();
   for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
-    int64_t off = 0;
+    int off = 0;
     for (int el = 0; el < p.E_r; ++el) {
-      p.expert_offset[r * p.E_r + el] = (int32_t)off;
-      const int64_t n = p.expert_count[r * p.E_r + el];
-      off += (n + kPadRows - 1) / kPadRows * kPadRows;
+      const int e = r * p.E_r + el;
+      p.expert_offset[e] = off;
+      s_off[e] = off;
+      off += (s_cnt[e] + kPadRows - 1) / kPadRows * kPadRows;
     }
-    p.rank_rows[r] = (int32_t)off;
+    p.rank_rows[r] = off;
+    s_base[r] = off;  // rank r's padded rows; turned into first pool rows below
   }
   __syncthreads();
   // ranks take consecutive regions of the pool shared by all ranks
   if (threadIdx.x == 0) {
     int64_t base = 0;
     for (int r = 0; r < p.R; ++r) {
+      const int rows = s_base[r];
+      s_base[r] = (int)base;
       p.rank_base[r] = (int32_t)base;
-      base += p.rank_rows[r];
+      base += rows;
     }
     if (base > p.pcap) atomicOr(p.err, kErrCapacity);
   }
   __syncthreads();
-  // padding rows carry src_info = -1
-  for (int64_t i = threadIdx.x; i < (int64_t)p.E * kPadRows; i += blockDim.x) {
-    const int e = (int)(i / kPadRows), q = (int)(i % kPadRows);
-    const int n = p.expert_count[e];
-    const int64_t row = (int64_t)p.expert_offset[e] + n + q;
-    const int64_t end = (int64_t)p.expert_offset[e] + (n + kPadRows - 1) / kPadRows * kPadRows;
-    const int64_t prow = p.rank_base[e / p.E_r] + row;
-    if (row < end && prow < p.pcap) p.packed_src_info[prow] = -1;
+  // padding rows carry src_info = -1: one warp per expert, a lane per row
+  for (int e = warp; e < p.E; e += kWarps) {
+    const int n = s_cnt[e];
+    const int npad = (n + kPadRows - 1) / kPadRows * kPadRows - n;
+    const int64_t row0 = (int64_t)s_base[e / p.E_r] + s_off[e] + n;
+    for (int q = lane; q < npad; q += 32)
+      if (row0 + q < p.pcap) p.packed_src_info[row0 + q] = -1;
   }
   if (threadIdx.x == 0) *p.ticket = 0u;
 }
@@ -235,6 +249,8 @@ cudaError_t launch_layout_2d(const LayoutParams& p, cudaStream_t st) {
 
 cudaError_t launch_layout_std(const LayoutParams& p, cudaStream_t st) {
   if (p.nchunks == 0) return cudaSuccess;
+  // per-warp expert bitmaps and prefixes; the last CTA reuses the space for
+  // two int arrays of E (8 E bytes <= 40 E bytes)
   const size_t smem = (size_t)kWarps * p.E * (sizeof(uint32_t) + 1);
   if (smem > 48 * 1024) (void)ctas_per_sm(layout_std_kernel, kLayoutThreads, smem);
   layout_std_kernel<<<p.nchunks, kLayoutThreads, smem, st>>>(p);
