@@ -638,9 +638,12 @@ def split_leg(wl, dev, K: int, W: int):
     """The split send / receive phases with every rank a handle on this GPU
     (User Guide, section 3, split dispatch/combine): dispatch = every rank's
     dispatch_send, then every rank's dispatch_recv; combine = every rank's
-    combine_send, then every rank's combine_recv; one stream orders the
-    phases. Bytes as for the single-workspace path (the same receive rows and
-    outputs), so GB/s compare directly; the send phase's staging is extra."""
+    combine_send (zero-copy: the expert outputs are in the registered
+    buffers), then every rank's combine_recv; one stream orders the phases.
+    Bytes as for the single-workspace path (the same receive rows and
+    outputs), so GB/s compare directly; the staging and the pull's second
+    copy of each row are extra. Eager timing includes the host's per-rank
+    launches; the graph timings replay each phase captured once."""
     from combine_route_layout_gb300 import EpDispatchCombineConfig
     from combine_route_layout_gb300.ranks import EpRankOp
     R, T = wl.world_size, wl.tokens_per_rank
@@ -672,8 +675,10 @@ def split_leg(wl, dev, K: int, W: int):
         return views
 
     def combine(views):
+        # zero-copy: the experts' outputs are already in each rank's registered
+        # combine input (written once below, outside the timed region)
         for r, op in enumerate(ops):
-            op.combine_send(y[r], views[r][1] if wl.weighted else None, out=outs[r],
+            op.combine_send(None, views[r][1] if wl.weighted else None, out=outs[r],
                             want_weights=False)
         for op in ops:
             op.combine_recv(call_reset=True)
@@ -681,6 +686,8 @@ def split_leg(wl, dev, K: int, W: int):
     views = dispatch()
     torch.cuda.synchronize()
     recv = torch.cat([v[4] for v in views]).cpu().numpy()
+    for r, op in enumerate(ops):
+        op.get_registered_combine_input_buffer()[:int(recv[r])].copy_(y[r, :int(recv[r])])
     combine(views)
     b = algorithmic_bytes(wl, int(recv.sum()), 0, int(ntok.sum()))
     small = int(ntok.sum()) * wl.hidden * 2 < 128 * 1024 * 1024
@@ -701,9 +708,39 @@ def split_leg(wl, dev, K: int, W: int):
         if it >= W:
             d_us.append(e[0].elapsed_time(e[1]) * 1e3)
             c_us.append(e[1].elapsed_time(e[2]) * 1e3)
+    # the same phases captured once into CUDA graphs and replayed: device time
+    # without the host's per-rank launch overhead
+    gd, gc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        combine(dispatch())
+    st.wait_stream(side)
+    torch.cuda.synchronize()
+    holder = {}
+    with torch.cuda.graph(gd):
+        holder["v"] = dispatch()
+    with torch.cuda.graph(gc):
+        combine(holder["v"])
+    gd_us, gc_us = [], []
+    for it in range(W + K):
+        if flush is not None:
+            torch.sum(flush, dim=0, out=sink)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(st)
+        gd.replay()
+        e[1].record(st)
+        gc.replay()
+        e[2].record(st)
+        torch.cuda.synchronize()
+        if it >= W:
+            gd_us.append(e[0].elapsed_time(e[1]) * 1e3)
+            gc_us.append(e[1].elapsed_time(e[2]) * 1e3)
     peak, _ = hbm_peak()
     rec = {"workload": wl.name, "ranks": R, "iters": K,
-           "l2": "flushed (256 MB read) before each step" if small else "inputs larger than L2"}
+           "l2": "flushed (256 MB read) before each step" if small else "inputs larger than L2",
+           "graph_dispatch_us_median": round(statistics.median(gd_us), 2),
+           "graph_combine_us_median": round(statistics.median(gc_us), 2)}
     for name, us in (("dispatch", d_us), ("combine", c_us)):
         med = statistics.median(us)
         gbs = b[name] / (med * 1e-6) / 1e9
