@@ -790,10 +790,14 @@ ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* com
   p.src_pos = h->w.src_pos;
   p.row_map = h->w.row_map;
   p.recv_rows = h->w.conv_recv_rows;
+  p.err = h->w.err;
   p.packed_y = static_cast<const uint8_t*>(packed_y);
   p.combine_in = static_cast<uint8_t*>(combine_in);
-  cudaError_t e = ep::launch_convert_combine(p, h->cfg.combine_dtype,
-                                             launch_cfg(h, EP_PHASE_COMBINE), st);
+  // the bulk-copy ring unless the vector kernel is asked for
+  const ep::LaunchCfg lc = launch_cfg(h, EP_PHASE_COMBINE);
+  cudaError_t e = h->cfg.combine_impl != EP_COMBINE_VECTOR && ep::convert_combine_bulk_supported(p)
+                      ? ep::launch_convert_combine_bulk(p, h->cfg.combine_dtype, lc, st)
+                      : ep::launch_convert_combine(p, h->cfg.combine_dtype, lc, st);
   if (e != cudaSuccess) return cuda_fail(e, "convert_combine_input launch");
   return EP_OK;
 }

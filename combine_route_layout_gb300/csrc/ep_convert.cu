@@ -15,6 +15,8 @@
 // sum of the token's packed rows on r (slots ascending), rounded once.
 #include <algorithm>
 
+#include "ep_bulk.cuh"
+#include "ep_combine_common.cuh"
 #include "ep_kernels.cuh"
 
 namespace ep {
@@ -293,7 +295,168 @@ __global__ void __launch_bounds__(256) conv_combine_kernel(ConvertParams p) {
   }
 }
 
+// convert_combine_input with bulk asynchronous copies (the TMA engine) into a
+// shared-memory ring; the same sums as conv_combine_kernel, bit for bit. A
+// unit is (present receive row, 1024-column chunk); CTA b takes present rows
+// b, b + G, ... (G CTAs) over all ranks, every chunk of each. One producer
+// warp reads a row's packed-row list once (the next row's is fetched
+// meanwhile) and, per chunk, has each lane holding a packed row issue one
+// cp.async.bulk of that row's chunk into the unit's stage, in slot order;
+// four consumer warps sum the stage's rows from shared memory from +0 in
+// slot order, round once and store the receive-row chunk. Four stages let
+// the producer run up to four units ahead, so row loads are in flight while
+// earlier units are summed, without holding them in registers. Waits are
+// bounded: on a timeout the kernel sets an error bit and returns.
+constexpr int kBCols = 1024;     // columns of one unit
+constexpr int kBStages = 4;      // units in flight per CTA
+constexpr int kBRows = 8;        // at most 8 packed rows per receive row
+constexpr int kBConsumers = 4;   // 128 consumer threads x 8 columns = kBCols
+constexpr int kBThreads = (kBConsumers + 1) * 32;
+
+struct alignas(16) ConvStage {
+  int64_t rowg;  // receive row r * cap + i
+  int seg;       // column chunk
+  int D;         // packed rows in the stage
+};
+
+template <int DT>
+struct alignas(128) ConvRing {
+  uint8_t data[kBStages][kBRows][kBCols * dt_size(DT)];
+  ConvStage hdr[kBStages];
+  uint64_t full[kBStages];
+  uint64_t empty[kBStages];
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kBThreads, 3) conv_combine_bulk_kernel(ConvertParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  ConvRing<DT>& ring = *reinterpret_cast<ConvRing<DT>*>(smem_raw);
+  constexpr int esz = dt_size(DT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int64_t pre[EP_MAX_WORLD_SIZE + 1];  // present receive rows before rank r
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(&ring.full[s], 1);
+      mbar_init(&ring.empty[s], kBConsumers);
+    }
+    mbar_init_fence();
+    pre[0] = 0;
+    for (int r = 0; r < p.R; ++r) {
+      const int n = __ldg(p.recv_num_token + r);
+      pre[r + 1] = pre[r] + (n < 0 ? 0 : (n > p.cap ? p.cap : n));
+    }
+  }
+  __syncthreads();
+  const int segs = (p.H + kBCols - 1) / kBCols;
+  const int64_t rows = pre[p.R];
+  const int64_t G = gridDim.x;
+  const int64_t nunits = (blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0) * segs;
+  auto rowg_of = [&](int64_t v) -> int64_t {  // v-th present receive row
+    int r = 0;
+    while (r + 1 < p.R && v >= pre[r + 1]) ++r;
+    return (int64_t)r * p.cap + (v - pre[r]);
+  };
+
+  if (warp == kBConsumers) {  // ------------------------------------ producer
+    auto prow_of = [&](int64_t v) -> int {  // packed row of slot `lane`, -1 if none
+      if (v >= rows || lane >= p.k) return -1;
+      return __ldg(p.recv_rows + rowg_of(v) * p.k + lane);
+    };
+    int i = 0;
+    bool failed = false;
+    int pr_next = prow_of(blockIdx.x);
+    for (int64_t v = blockIdx.x; v < rows && !failed; v += G) {
+      const int64_t rowg = rowg_of(v);
+      const int pr = pr_next;
+      pr_next = prow_of(v + G);  // the next row's list is fetched meanwhile
+      const uint32_t m = __ballot_sync(kFull, pr >= 0);
+      const int d = pr >= 0 ? __popc(m & lanemask_lt()) : -1;  // slot order
+      const int D = __popc(m);
+      for (int seg = 0; seg < segs; ++seg, ++i) {
+        const int st = i % kBStages;
+        const uint32_t ph = (uint32_t)(i / kBStages) & 1u;
+        if (i >= kBStages && !mbar_wait(&ring.empty[st], ph ^ 1u)) {
+          if (lane == 0) atomicOr(p.err, kErrTimeout);
+          failed = true;
+          break;
+        }
+        const uint32_t bytes = (uint32_t)(min(kBCols, p.H - seg * kBCols) * esz);
+        if (lane == 0) {
+          ring.hdr[st].rowg = rowg;
+          ring.hdr[st].seg = seg;
+          ring.hdr[st].D = D;
+          mbar_arrive_expect_tx(&ring.full[st], (uint32_t)D * bytes);
+        }
+        __syncwarp();
+        if (d >= 0)
+          bulk_g2s(ring.data[st][d], p.packed_y + ((int64_t)pr * p.H + (int64_t)seg * kBCols) * esz,
+                   bytes, &ring.full[st]);
+      }
+    }
+    // Do not leave while copies into this CTA's shared memory may be in flight.
+    if (lane == 0) {
+      for (int j = i - kBStages; j < i; ++j) {
+        if (j < 0) continue;
+        if (!mbar_wait(&ring.full[j % kBStages], (uint32_t)(j / kBStages) & 1u)) {
+          atomicOr(p.err, kErrTimeout);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------------- consumers
+  const int tid = threadIdx.x;  // 0 .. 127
+  for (int i = 0; i < nunits; ++i) {
+    const int st = i % kBStages;
+    if (!mbar_wait(&ring.full[st], (uint32_t)(i / kBStages) & 1u)) {
+      if (lane == 0) atomicOr(p.err, kErrTimeout);
+      return;
+    }
+    const ConvStage h = ring.hdr[st];
+    const int col = h.seg * kBCols + tid * 8;
+    if (col < p.H) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+      for (int d = 0; d < kBRows; ++d) {
+        if (d < h.D) {
+          const uint8_t* src = ring.data[st][d] + tid * 8 * esz;
+          Raw8<DT> raw;
+          raw.a = ld_shared_v4(src);
+          if (DT != EP_DTYPE_BF16) raw.b = ld_shared_v4(src + 16);
+          float f[8];
+          unpack8<DT>(raw, f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+        }
+      }
+      store8<DT>(p.combine_in + h.rowg * p.H * esz, col, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[st]);
+  }
+}
+
 }  // namespace
+
+bool convert_combine_bulk_supported(const ConvertParams& p) { return p.k <= kBRows; }
+
+cudaError_t launch_convert_combine_bulk(const ConvertParams& p, int dtype, const LaunchCfg& lc,
+                                        cudaStream_t st) {
+  if (p.total_units == 0) return cudaSuccess;
+  const bool bf = dtype == EP_DTYPE_BF16;
+  auto k = bf ? conv_combine_bulk_kernel<EP_DTYPE_BF16> : conv_combine_bulk_kernel<EP_DTYPE_FP32>;
+  const size_t smem = bf ? sizeof(ConvRing<EP_DTYPE_BF16>) : sizeof(ConvRing<EP_DTYPE_FP32>);
+  const int per_sm = ctas_per_sm(k, kBThreads, smem);  // also raises the smem limit
+  int64_t grid = lc.grid_hint > 0 ? lc.grid_hint : (int64_t)lc.sm_count * per_sm;
+  const int64_t rows = (int64_t)p.R * p.cap;  // upper bound of the present rows
+  if (grid > rows) grid = rows;
+  k<<<(unsigned)grid, kBThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
                                     const LaunchCfg& lc, cudaStream_t st) {

@@ -65,7 +65,7 @@ typedef enum {
 
 typedef enum {
     EP_COMBINE_AUTO = 0,        /* bulk for the 2D layout from 8192 source tokens on,
-                                   vector otherwise */
+                                   vector otherwise; convert_combine_input: bulk */
     EP_COMBINE_VECTOR = 1,      /* 16-byte vector loads into registers */
     EP_COMBINE_BULK = 2         /* bulk async copies (TMA) into a shared-memory ring; needs
                                    <= 8 rows per token (world_size <= 8, or top-k <= 8
@@ -299,7 +299,10 @@ ep_status ep_convert_dispatch_output(ep_handle* h, const void* dispatch_x,
  * order, of their packed rows, rounded once to combine_dtype.
  *   packed_y    device [pcap][H] combine_dtype, in the packed pool's rows
  *   combine_in  device [R][cap][H] combine_dtype (rows past recv_num_token untouched)
- * Needs both layouts (ep_dispatch, then ep_convert_dispatch_output).
+ * Needs both layouts (ep_dispatch, then ep_convert_dispatch_output). Runs
+ * the bulk-copy kernel unless the combine phase is set to EP_COMBINE_VECTOR
+ * (or top-k > 8); both give the same bits. A bounded wait that gives up sets
+ * the timeout bit reported by ep_sync.
  */
 ep_status ep_convert_combine_input(ep_handle* h, const void* packed_y, void* combine_in,
                                    void* stream);

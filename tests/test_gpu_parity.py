@@ -325,13 +325,16 @@ def test_skewed_std_full_size():
 
 # ------------------------------------------------------------- conversions
 
-def test_convert_round_trip():
-    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=260, hidden=1024, mask_prob=0.1)
+def run_convert(wl, seed, impl="auto", dtype=torch.bfloat16):
+    """dispatch -> convert_dispatch_output -> convert_combine_input -> combine
+    (and combine_standard_moe on the converted layout), every row against the
+    oracle. impl picks the convert_combine_input kernel (combine phase)."""
     R, T, H, Er, k = wl.world_size, wl.tokens_per_rank, wl.hidden, wl.experts_per_rank, wl.topk
-    inp = Inputs(wl, 3, ragged=True)
-    cfg = make_config(wl, standard_moe=2, combine_dtype=torch.bfloat16,
+    inp = Inputs(wl, seed, ragged=True)
+    cfg = make_config(wl, standard_moe=2, combine_dtype=dtype,
                       combine_out_dtype=torch.float32, weighted_combine=False)
     op = EpDispatchCombineOp(cfg)
+    op.set_launch_config(E.EP_PHASE_COMBINE, impl)
     d_x, d_w, _, d_idx, recv_d = op.dispatch(inp.x, inp.w_d, None, inp.idx_d, inp.ntok)
     px, pcount, psrc, prange = op.convert_dispatch_output(d_x, d_idx)
     op.sync()
@@ -350,11 +353,12 @@ def test_convert_round_trip():
         assert np.array_equal(gx[r, :n][used], ref["x"][r, :n][used])
 
     recv, src_pos, slot = oracle.route(inp.idx, inp.ntok, Er)
-    Y = _pool_y(wl, op.pcap, 3)
+    Y = _pool_y(wl, op.pcap, seed, dtype=dtype)
     y2d = op.convert_combine_input(Y, psrc, prange)
+    op.sync()
     Yh = pool_to_ranks(host(Y), base, ref["rank_rows"], pcap)
     y2d_ref = oracle.convert_combine_input(Yh, recv, src_pos, inp.idx, ref["row_map"], Er,
-                                           out_dtype="bf16")
+                                           out_dtype="bf16" if dtype == torch.bfloat16 else "fp32")
     gy = host(y2d)
     for r in range(R):
         assert np.array_equal(gy[r, :recv[r]], y2d_ref[r, :recv[r]]), f"convert_combine_input {r}"
@@ -372,6 +376,34 @@ def test_convert_round_trip():
     for s in range(R):
         n = inp.ntok[s]
         assert np.array_equal(gs[s, :n].view(np.uint32), ref_std[s, :n].view(np.uint32))
+
+
+@pytest.mark.parametrize("impl,hidden,dtype,seed", [
+    ("auto", 1024, torch.bfloat16, 3),
+    ("vector", 1024, torch.bfloat16, 3),
+    ("bulk", 1056, torch.bfloat16, 4),     # a ragged last column chunk
+    ("vector", 1056, torch.bfloat16, 4),
+    ("bulk", 2080, torch.float32, 5),      # f32 rows, three chunks
+    ("vector", 2080, torch.float32, 5),
+])
+def test_convert_round_trip(impl, hidden, dtype, seed):
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(tokens_per_rank=260, hidden=hidden, mask_prob=0.1)
+    run_convert(wl, seed, impl, dtype)
+
+
+def test_convert_round_trip_top2_sixteen_ranks():
+    """Few slots per token over many ranks: many receive rows with one
+    packed row each and rows with none on a rank."""
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(world_size=16, experts_per_rank=4, topk=2,
+                                               tokens_per_rank=150, hidden=512, mask_prob=0.2)
+    run_convert(wl, 6, "bulk")
+
+
+@pytest.mark.slow
+def test_convert_full_size():
+    """The skewed shape whole (8 x 4096 tokens, H 7168) through both
+    conversions, every receive row and packed row compared."""
+    run_convert(WORKLOADS["skewed_zipf_std_moe"], 7, "auto")
 
 
 # ------------------------------------------------------------ error flags
