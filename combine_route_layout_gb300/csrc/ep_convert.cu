@@ -156,13 +156,26 @@ __global__ void __launch_bounds__(256, 4) conv_copy_kernel(ConvertParams p) {
   const int E = p.R * p.E_r;
   const int64_t stride = (int64_t)p.R * p.Tmax;  // src_token_pos rank stride
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < p.total_units;
+  // units run over the present receive rows only: row `row` of the ranks'
+  // concatenated rows is row row - pre[r] of rank r
+  __shared__ int64_t pre[EP_MAX_WORLD_SIZE + 1];
+  if (threadIdx.x == 0) {
+    pre[0] = 0;
+    for (int r = 0; r < p.R; ++r) {
+      const int n = __ldg(p.recv_num_token + r);
+      pre[r + 1] = pre[r] + (n < 0 ? 0 : (n > p.cap ? p.cap : n));
+    }
+  }
+  __syncthreads();
+  const int64_t units = pre[p.R] * p.segs_per_row;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < units;
        u += nwarps) {
-    const int64_t rowg = u / p.segs_per_row;  // r * cap + i
-    const int seg = (int)(u - rowg * p.segs_per_row);
-    const int r = (int)(rowg / p.cap);
-    const int64_t i = rowg - (int64_t)r * p.cap;
-    if (i >= __ldg(p.recv_num_token + r)) continue;
+    const int64_t row = u / p.segs_per_row;
+    const int seg = (int)(u - row * p.segs_per_row);
+    int r = 0;
+    while (r + 1 < p.R && row >= pre[r + 1]) ++r;
+    const int64_t i = row - pre[r];
+    const int64_t rowg = (int64_t)r * p.cap + i;  // r * cap + i
 
     const uint8_t* src = p.recv_x + rowg * p.row_bytes;
     uint4 v[kCopyUnroll];
