@@ -14,6 +14,7 @@
 #include <string>
 #include <tuple>
 
+#include "ep_convert.cuh"
 #include "ep_kernels.cuh"
 
 namespace {

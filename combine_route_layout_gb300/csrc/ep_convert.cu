@@ -17,6 +17,7 @@
 
 #include "ep_bulk.cuh"
 #include "ep_combine_common.cuh"
+#include "ep_convert.cuh"
 #include "ep_kernels.cuh"
 
 namespace ep {

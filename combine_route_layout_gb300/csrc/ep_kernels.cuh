@@ -258,10 +258,6 @@ cudaError_t launch_convert_dispatch(const ConvertParams& p, bool with_scales,
                                     const LaunchCfg& lc, cudaStream_t st);
 cudaError_t launch_convert_combine(const ConvertParams& p, int dtype, const LaunchCfg& lc,
                                    cudaStream_t st);
-// convert_combine_input through the bulk-copy ring (k <= 8).
-bool convert_combine_bulk_supported(const ConvertParams& p);
-cudaError_t launch_convert_combine_bulk(const ConvertParams& p, int dtype, const LaunchCfg& lc,
-                                        cudaStream_t st);
 
 // Split phases (ep_split.cu). quant as for launch_dispatch_2d.
 cudaError_t launch_split_stage(const SplitParams& p, int quant, const LaunchCfg& lc,
