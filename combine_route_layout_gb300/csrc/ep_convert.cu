@@ -18,6 +18,7 @@
 #include "ep_bulk.cuh"
 #include "ep_combine_common.cuh"
 #include "ep_convert.cuh"
+#include "ep_ids.cuh"
 #include "ep_kernels.cuh"
 
 namespace ep {
@@ -50,9 +51,10 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
   for (int q = threadIdx.x; q < kWarps * p.E_r; q += blockDim.x) bits[q] = 0u;
   __syncthreads();
   const uint32_t me = 1u << lane;
+  int ids[kIdsMax];
+  const bool held = valid && load_ids(p.recv_idx + row * p.k, p.k, ids);  // kept for the 2nd pass
   if (valid) {
-    for (int j = 0; j < p.k; ++j) {
-      const int e = __ldg(p.recv_idx + row * p.k + j);
+    auto take = [&](int j, int e) {
       uint16_t mark = 0xFFFFu;
       if (e < -1 || e >= E) {
         atomicOr(p.err, kErrIndex);
@@ -62,6 +64,13 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
         else mark = 0;
       }
       p.local16[row * p.k + j] = mark;
+    };
+    if (held) {
+#pragma unroll
+      for (int j = 0; j < kIdsMax; ++j)
+        if (j < p.k) take(j, ids[j]);
+    } else {
+      for (int j = 0; j < p.k; ++j) take(j, __ldg(p.recv_idx + row * p.k + j));
     }
   }
   __syncthreads();
@@ -77,13 +86,19 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
   __syncthreads();
   if (valid) {
     const uint32_t lt = lanemask_lt();
-    for (int j = 0; j < p.k; ++j) {
-      const int e = __ldg(p.recv_idx + row * p.k + j);
-      if (e < 0 || e >= E || e / p.E_r != r) continue;
-      if (p.local16[row * p.k + j] != 0u) continue;
+    auto place = [&](int j, int e) {
+      if (e < 0 || e >= E || e / p.E_r != r) return;
+      if (p.local16[row * p.k + j] != 0u) return;
       const int el = e % p.E_r;
       p.local16[row * p.k + j] =
           (uint16_t)(pre[warp * p.E_r + el] + __popc(bits[warp * p.E_r + el] & lt));
+    };
+    if (held) {
+#pragma unroll
+      for (int j = 0; j < kIdsMax; ++j)
+        if (j < p.k) place(j, ids[j]);
+    } else {
+      for (int j = 0; j < p.k; ++j) place(j, __ldg(p.recv_idx + row * p.k + j));
     }
   }
 

@@ -18,6 +18,7 @@
 // shared memory, and the last CTA also lays out the 128-row padded expert
 // segments, the per-source-rank layout ranges and each rank's first row in
 // the packed pool the ranks share (the prefix of their padded row counts).
+#include "ep_ids.cuh"
 #include "ep_kernels.cuh"
 
 namespace ep {
@@ -50,14 +51,21 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_2d_kernel(LayoutParams 
   uint32_t m = 0;
   if (valid) {
     const int32_t* row = p.idx + g * p.k;
-    for (int j = 0; j < p.k; ++j) {
-      const int e = __ldg(row + j);
-      if (e == -1) continue;
+    auto take = [&](int e) {
+      if (e == -1) return;
       if (e < -1 || e >= p.E) {
         atomicOr(p.err, kErrIndex);
-        continue;
+        return;
       }
       m |= 1u << (e / p.E_r);
+    };
+    int ids[kIdsMax];
+    if (load_ids(row, p.k, ids)) {
+#pragma unroll
+      for (int j = 0; j < kIdsMax; ++j)
+        if (j < p.k) take(ids[j]);
+    } else {
+      for (int j = 0; j < p.k; ++j) take(__ldg(row + j));
     }
     p.mask[g] = m;
   }
@@ -128,10 +136,11 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
   for (int i = threadIdx.x; i < kWarps * p.E; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
   const uint32_t me = 1u << lane;
+  int ids[kIdsMax];
+  const bool held = valid && load_ids(p.idx + g * p.k, p.k, ids);  // ids kept for the 2nd pass
   if (valid) {
     const int32_t* row = p.idx + g * p.k;
-    for (int j = 0; j < p.k; ++j) {
-      const int e = __ldg(row + j);
+    auto take = [&](int j, int e) {
       uint16_t mark = 0xFFFFu;
       if (e < -1 || e >= p.E) {
         atomicOr(p.err, kErrIndex);
@@ -141,6 +150,13 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
         else mark = 0;
       }
       p.local16[g * p.k + j] = mark;  // 0 = counted (filled in below), 0xFFFF = no row
+    };
+    if (held) {
+#pragma unroll
+      for (int j = 0; j < kIdsMax; ++j)
+        if (j < p.k) take(j, ids[j]);
+    } else {
+      for (int j = 0; j < p.k; ++j) take(j, __ldg(row + j));
     }
   }
   __syncthreads();
@@ -157,12 +173,18 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
   if (valid) {
     const uint32_t lt = lanemask_lt();
     const int32_t* row = p.idx + g * p.k;
-    for (int j = 0; j < p.k; ++j) {
-      const int e = __ldg(row + j);
-      if (e < 0 || e >= p.E) continue;
-      if (p.local16[g * p.k + j] != 0u) continue;  // duplicate already marked
+    auto place = [&](int j, int e) {
+      if (e < 0 || e >= p.E) return;
+      if (p.local16[g * p.k + j] != 0u) return;  // duplicate already marked
       p.local16[g * p.k + j] =
           (uint16_t)(pre[warp * p.E + e] + __popc(bits[warp * p.E + e] & lt));
+    };
+    if (held) {
+#pragma unroll
+      for (int j = 0; j < kIdsMax; ++j)
+        if (j < p.k) place(j, ids[j]);
+    } else {
+      for (int j = 0; j < p.k; ++j) place(j, __ldg(row + j));
     }
   }
 
