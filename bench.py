@@ -639,11 +639,14 @@ def split_leg(wl, dev, K: int, W: int):
     (User Guide, section 3, split dispatch/combine): dispatch = every rank's
     dispatch_send, then every rank's dispatch_recv; combine = every rank's
     combine_send (zero-copy: the expert outputs are in the registered
-    buffers), then every rank's combine_recv; one stream orders the phases.
-    Bytes as for the single-workspace path (the same receive rows and
-    outputs), so GB/s compare directly; the staging and the pull's second
-    copy of each row are extra. Eager timing includes the host's per-rank
-    launches; the graph timings replay each phase captured once."""
+    buffers), then every rank's combine_recv. Every rank runs on a stream of
+    its own, as ranks on separate GPUs would run side by side; a phase ends
+    when all ranks' streams have finished it (events), and no kernel waits
+    on another rank's. Bytes as for the single-workspace path (the same
+    receive rows and outputs), so GB/s compare directly; the staging and the
+    pull's second copy of each row are extra. Eager timing includes the
+    host's per-rank launches; the graph timings replay each phase captured
+    once."""
     from combine_route_layout_gb300 import EpDispatchCombineConfig
     from combine_route_layout_gb300.ranks import EpRankOp
     R, T = wl.world_size, wl.tokens_per_rank
@@ -667,21 +670,32 @@ def split_leg(wl, dev, K: int, W: int):
     y = make_expert_outputs(wl, R * T, 0, device=dev)
     outs = [torch.empty((T, wl.hidden), dtype=cfg.combine_out_dtype, device=dev) for _ in range(R)]
 
+    lanes = [torch.cuda.Stream(device=dev) for _ in range(R)]
+
+    def phase(fn):
+        """fn(r, op) on every rank's stream, after all work so far on the
+        current stream; the current stream then waits for every rank."""
+        cur = torch.cuda.current_stream()
+        out = []
+        for r, op in enumerate(ops):
+            lanes[r].wait_stream(cur)
+            with torch.cuda.stream(lanes[r]):
+                out.append(fn(r, op))
+        for ln in lanes:
+            cur.wait_stream(ln)
+        return out
+
     def dispatch():
-        views = [op.dispatch_send(x[r], w[r], None, idx[r], int(ntok[r]))
-                 for r, op in enumerate(ops)]
-        for op in ops:
-            op.dispatch_recv()
+        views = phase(lambda r, op: op.dispatch_send(x[r], w[r], None, idx[r], int(ntok[r])))
+        phase(lambda r, op: op.dispatch_recv())
         return views
 
     def combine(views):
         # zero-copy: the experts' outputs are already in each rank's registered
         # combine input (written once below, outside the timed region)
-        for r, op in enumerate(ops):
-            op.combine_send(None, views[r][1] if wl.weighted else None, out=outs[r],
-                            want_weights=False)
-        for op in ops:
-            op.combine_recv(call_reset=True)
+        phase(lambda r, op: op.combine_send(None, views[r][1] if wl.weighted else None,
+                                            out=outs[r], want_weights=False))
+        phase(lambda r, op: op.combine_recv(call_reset=True))
 
     views = dispatch()
     torch.cuda.synchronize()
@@ -741,12 +755,20 @@ def split_leg(wl, dev, K: int, W: int):
            "l2": "flushed (256 MB read) before each step" if small else "inputs larger than L2",
            "graph_dispatch_us_median": round(statistics.median(gd_us), 2),
            "graph_combine_us_median": round(statistics.median(gc_us), 2)}
-    for name, us in (("dispatch", d_us), ("combine", c_us)):
+    # eager: each phase issued rank by rank from Python (16 library calls and
+    # their stream forks per step), so at small sizes the host sets the pace;
+    # graph: the device time of the same phases
+    for name, us, gus in (("dispatch", d_us, gd_us), ("combine", c_us, gc_us)):
         med = statistics.median(us)
         gbs = b[name] / (med * 1e-6) / 1e9
+        gmed = statistics.median(gus)
+        ggbs = b[name] / (gmed * 1e-6) / 1e9
         rec[name] = {"us_median": round(med, 2), "us_p10": round(pctl(us, 10), 2),
                      "us_p90": round(pctl(us, 90), 2), "GBps": round(gbs, 1),
-                     "frac_of_peak": round(gbs / peak, 4)}
+                     "frac_of_peak": round(gbs / peak, 4),
+                     "graph_us_median": round(gmed, 2), "graph_us_p10": round(pctl(gus, 10), 2),
+                     "graph_us_p90": round(pctl(gus, 90), 2), "graph_GBps": round(ggbs, 1),
+                     "graph_frac_of_peak": round(ggbs / peak, 4)}
     return rec
 
 

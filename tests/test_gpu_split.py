@@ -22,35 +22,49 @@ from split_worker import DEV, Group, config, run_process_rank
 pytestmark = pytest.mark.gpu
 
 
-def run_inprocess(wl, seed=0, ragged=False, zero_copy=False, rounds=1, **cfg_over):
+def run_inprocess(wl, seed=0, ragged=False, zero_copy=False, rounds=1, streams=False,
+                  **cfg_over):
+    """Every rank a handle. One stream orders the phases, or (streams=True)
+    every rank runs on a stream of its own and a phase ends when all ranks'
+    streams have finished it, as ranks on separate GPUs would run."""
     from combine_route_layout_gb300.ranks import EpRankOp
     R = wl.world_size
     ops = [EpRankOp(config(wl, **cfg_over), r) for r in range(R)]
     ptrs = [op.workspace.data_ptr() for op in ops]
     for op in ops:
         op.set_peers(ptrs)
+    lanes = [torch.cuda.Stream() for _ in range(R)] if streams else None
+
+    def phase(fn):
+        if not streams:
+            return [fn(r, op) for r, op in enumerate(ops)]
+        cur = torch.cuda.current_stream()
+        out = []
+        for r, op in enumerate(ops):
+            lanes[r].wait_stream(cur)
+            with torch.cuda.stream(lanes[r]):
+                out.append(fn(r, op))
+        for ln in lanes:
+            cur.wait_stream(ln)
+        return out
+
     for it in range(rounds):
         g = Group(wl, seed + it, ragged)
-        views = []
-        for r, op in enumerate(ops):
-            x, w, idx = g.inputs(r)
-            views.append(op.dispatch_send(x, w, None, idx, int(g.ntok[r])))
-        for op in ops:
-            op.dispatch_recv()
+        ins = [g.inputs(r) for r in range(R)]
+        views = phase(lambda r, op: op.dispatch_send(ins[r][0], ins[r][1], None, ins[r][2],
+                                                     int(g.ntok[r])))
+        phase(lambda r, op: op.dispatch_recv())
         torch.cuda.synchronize()
         for r, op in enumerate(ops):
             g.check_dispatch(r, views[r], op.get_dispatch_src_token_pos())
-        outs = []
-        for r, op in enumerate(ops):
-            n = int(g.recv[r])
-            y = torch.from_numpy(g.yb[r].view(np.int16)).to(DEV).view(torch.bfloat16)
-            if zero_copy:
-                op.get_registered_combine_input_buffer()[:n].copy_(y[:n])
-                outs.append(op.combine_send(None, views[r][1]))
-            else:
-                outs.append(op.combine_send(y, views[r][1]))
-        for op in ops:
-            op.combine_recv(call_reset=True)
+        ys = [torch.from_numpy(g.yb[r].view(np.int16)).to(DEV).view(torch.bfloat16)
+              for r in range(R)]
+        if zero_copy:
+            for r, op in enumerate(ops):
+                n = int(g.recv[r])
+                op.get_registered_combine_input_buffer()[:n].copy_(ys[r][:n])
+        outs = phase(lambda r, op: op.combine_send(None if zero_copy else ys[r], views[r][1]))
+        phase(lambda r, op: op.combine_recv(call_reset=True))
         for op in ops:
             op.sync()
         for s in range(R):
@@ -78,6 +92,18 @@ def test_split_phases_zero_copy_and_repeated_rounds():
     rounds on the same handles with different routings and token counts."""
     wl = WORKLOADS["ds_v3_latency"].with_(tokens_per_rank=80, hidden=1024)
     run_inprocess(wl, seed=11, ragged=True, zero_copy=True, rounds=3)
+
+
+@pytest.mark.parametrize("name,over,seed,zero_copy", [
+    ("ds_v3_latency", dict(), 12, True),                                     # FP8, decode shape
+    ("mid_masked", dict(tokens_per_rank=300, hidden=1024, weighted=True,
+                        combine_out_dtype="fp32"), 13, False),
+])
+def test_split_phases_one_stream_per_rank(name, over, seed, zero_copy):
+    """Every rank's phase on its own stream, the ranks' kernels running side
+    by side (as bench.py --split times them); two rounds."""
+    run_inprocess(WORKLOADS[name].with_(**over), seed=seed, ragged=True, zero_copy=zero_copy,
+                  rounds=2, streams=True)
 
 
 def test_split_phases_decode_shape():
