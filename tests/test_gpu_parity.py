@@ -399,6 +399,14 @@ def test_convert_round_trip_top2_sixteen_ranks():
     run_convert(wl, 6, "bulk")
 
 
+def test_convert_round_trip_top12():
+    """More than 8 slots per token: convert_combine_input falls back from the
+    bulk ring (8 rows per unit) to the vector kernel under AUTO."""
+    wl = WORKLOADS["skewed_zipf_std_moe"].with_(topk=12, tokens_per_rank=120, hidden=768,
+                                               mask_prob=0.1)
+    run_convert(wl, 8, "auto")
+
+
 @pytest.mark.slow
 def test_convert_full_size():
     """The skewed shape whole (8 x 4096 tokens, H 7168) through both
