@@ -285,6 +285,30 @@ def time_steps(step: Step, K: int, W: int, flush: torch.Tensor | None, dist_barr
     return total_ms, disp, comb
 
 
+def event_floor_us(dev, iters: int, flush: torch.Tensor) -> dict:
+    """What CUDA events read around one and around two back-to-back
+    one-element kernels, after the same L2-evicting read as the decode-shape
+    steps: the fixed launch and event cost inside every such measurement."""
+    a = torch.zeros(1, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    out = {}
+    for n in (1, 2):
+        ts = []
+        for i in range(iters + 5):
+            torch.sum(flush, dim=0, out=sink)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(n):
+                a.add_(1.0)
+            e1.record(st)
+            torch.cuda.synchronize()
+            if i >= 5:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        out[f"{n}_kernel{'s' if n > 1 else ''}_us_median"] = round(statistics.median(ts), 2)
+    return out
+
+
 def graph_step_times(step: Step, iters: int, flush: torch.Tensor):
     """Dispatch + combine captured once into a CUDA graph and replayed, with an
     L2-evicting read before each replay; returns per-replay device times (µs)."""
@@ -987,6 +1011,9 @@ def main():
             "graph_step_us": round(statistics.median(graph_us), 2),
             "graph_step_GBps": round((lb["dispatch"] + lb["combine"])
                                      / (statistics.median(graph_us) * 1e-6) / 1e9, 1),
+            # events around near-empty kernels under the same protocol (dispatch
+            # launches two kernels, combine one)
+            "event_floor": event_floor_us(dev, lk, flush),
         }
         del ls, flush
 
