@@ -244,16 +244,17 @@ __global__ void __launch_bounds__(256, 4) conv_copy_kernel(ConvertParams p) {
   }
 }
 
-// layout_range[r][el][s] from the sorted src_info of each expert segment.
+// layout_range[r][el][s] from the sorted src_info of each expert segment:
+// thread (r, el, s) finds the first row of source s by binary search; the
+// rows of s end where those of s + 1 begin, which the next lane found (a
+// shuffle; lane 31 searches for itself), or at the segment's end.
 __global__ void conv_range_kernel(ConvertParams p) {
   const int64_t stride = (int64_t)p.R * p.Tmax;
   const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (q >= (int64_t)p.R * p.E_r * p.R) return;
-  const int s = (int)(q % p.R);
-  const int e = (int)(q / p.R);  // r * E_r + el
-  const int r = e / p.E_r;
-  const int32_t* seg = p.packed_src_info + (int64_t)p.rank_base[r] + p.expert_offset[e];
-  const int n = p.expert_count[e];
+  const int lane = threadIdx.x & 31;
+  const bool live = q < (int64_t)p.R * p.E_r * p.R;
+  int s = 0, n = 0, b = 0;
+  const int32_t* seg = nullptr;
   auto lower = [&](int64_t key) {
     int lo = 0, hi = n;
     while (lo < hi) {
@@ -263,7 +264,16 @@ __global__ void conv_range_kernel(ConvertParams p) {
     }
     return lo;
   };
-  const int b = lower((int64_t)s * stride), en = lower((int64_t)(s + 1) * stride);
+  if (live) {
+    s = (int)(q % p.R);
+    const int e = (int)(q / p.R);  // r * E_r + el
+    seg = p.packed_src_info + (int64_t)p.rank_base[e / p.E_r] + p.expert_offset[e];
+    n = p.expert_count[e];
+    b = s == 0 ? 0 : lower((int64_t)s * stride);
+  }
+  const int next_b = __shfl_down_sync(kFull, b, 1);
+  if (!live) return;
+  const int en = s == p.R - 1 ? n : lane < 31 ? next_b : lower((int64_t)(s + 1) * stride);
   p.layout_range[q] = (int64_t)(((uint64_t)(uint32_t)b << 32) | (uint32_t)(en - b));
 }
 
