@@ -53,17 +53,16 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
   const uint32_t me = 1u << lane;
   int ids[kIdsMax];
   const bool held = valid && load_ids(p.recv_idx + row * p.k, p.k, ids);  // kept for the 2nd pass
+  uint32_t counted = 0;  // bit j: slot j holds a row on this rank (written in the 2nd pass)
   if (valid) {
     auto take = [&](int j, int e) {
-      uint16_t mark = 0xFFFFu;
       if (e < -1 || e >= E) {
         atomicOr(p.err, kErrIndex);
       } else if (e >= 0 && e / p.E_r == r) {
         const uint32_t old = atomicOr(&bits[warp * p.E_r + e % p.E_r], me);
         if (old & me) atomicOr(p.err, kErrDuplicate);
-        else mark = 0;
+        else counted |= 1u << j;
       }
-      p.local16[row * p.k + j] = mark;
     };
     if (held) {
 #pragma unroll
@@ -87,11 +86,12 @@ __global__ void __launch_bounds__(kLayoutThreads) conv_layout_kernel(ConvertPara
   if (valid) {
     const uint32_t lt = lanemask_lt();
     auto place = [&](int j, int e) {
-      if (e < 0 || e >= E || e / p.E_r != r) return;
-      if (p.local16[row * p.k + j] != 0u) return;
-      const int el = e % p.E_r;
-      p.local16[row * p.k + j] =
-          (uint16_t)(pre[warp * p.E_r + el] + __popc(bits[warp * p.E_r + el] & lt));
+      uint16_t v = 0xFFFFu;  // no row on this rank (absent, dropped or repeated id)
+      if ((counted >> j) & 1u) {
+        const int el = e % p.E_r;
+        v = (uint16_t)(pre[warp * p.E_r + el] + __popc(bits[warp * p.E_r + el] & lt));
+      }
+      p.local16[row * p.k + j] = v;
     };
     if (held) {
 #pragma unroll

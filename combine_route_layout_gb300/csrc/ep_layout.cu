@@ -138,18 +138,17 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
   const uint32_t me = 1u << lane;
   int ids[kIdsMax];
   const bool held = valid && load_ids(p.idx + g * p.k, p.k, ids);  // ids kept for the 2nd pass
+  uint32_t counted = 0;  // bit j: slot j gets a row (its rank is written in the 2nd pass)
   if (valid) {
     const int32_t* row = p.idx + g * p.k;
     auto take = [&](int j, int e) {
-      uint16_t mark = 0xFFFFu;
       if (e < -1 || e >= p.E) {
         atomicOr(p.err, kErrIndex);
       } else if (e >= 0) {
         const uint32_t old = atomicOr(&bits[warp * p.E + e], me);
         if (old & me) atomicOr(p.err, kErrDuplicate);  // repeated id: later slot dropped
-        else mark = 0;
+        else counted |= 1u << j;
       }
-      p.local16[g * p.k + j] = mark;  // 0 = counted (filled in below), 0xFFFF = no row
     };
     if (held) {
 #pragma unroll
@@ -174,10 +173,9 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_std_kernel(LayoutParams
     const uint32_t lt = lanemask_lt();
     const int32_t* row = p.idx + g * p.k;
     auto place = [&](int j, int e) {
-      if (e < 0 || e >= p.E) return;
-      if (p.local16[g * p.k + j] != 0u) return;  // duplicate already marked
-      p.local16[g * p.k + j] =
-          (uint16_t)(pre[warp * p.E + e] + __popc(bits[warp * p.E + e] & lt));
+      uint16_t v = 0xFFFFu;  // no row: dropped, invalid or repeated id
+      if ((counted >> j) & 1u) v = (uint16_t)(pre[warp * p.E + e] + __popc(bits[warp * p.E + e] & lt));
+      p.local16[g * p.k + j] = v;
     };
     if (held) {
 #pragma unroll
