@@ -1035,6 +1035,9 @@ def main():
             wk[name] = time_workload(WORKLOADS[name], dev, max(50, min(K, 100)), args.warmup,
                                      args.cpu_reps, not args.no_cpu_baseline and world == 1)
         line["workloads"] = wk
+        # the packed layout reached through the 2D path: both conversions on
+        # the Zipf-skewed shape
+        line["convert_path"] = convert_leg(WORKLOADS["skewed_zipf_std_moe"], dev, 20, 3)
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_tokens, args.cpu_reps)
     if rank == 0:
