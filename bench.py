@@ -1038,6 +1038,9 @@ def main():
         # the packed layout reached through the 2D path: both conversions on
         # the Zipf-skewed shape
         line["convert_path"] = convert_leg(WORKLOADS["skewed_zipf_std_moe"], dev, 20, 3)
+        # the split send / receive phases, every rank a workspace of its own
+        line["split_path"] = [split_leg(WORKLOADS[n], dev, 20, 3)
+                              for n in ("ds_v3_latency", "ds_v3_throughput")]
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_tokens, args.cpu_reps)
     if rank == 0:
